@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the DCN core op (forward + backward) on one or more GPUs.
+
+A step is one pass of the whole op over one batch: the fused forward and the
+backward (grad_input, grad_offset, grad_mask) at the FlashInternImage-T
+stage-1 shape (N=64, 56x56, C=64, G=4, gc=16, 3x3, DCNv4 weights, float16
+storage), on seeded synthetic inputs already resident in HBM.
+
+  value     = ideal bytes of the step / device time of the step, in GB/s, over
+              all ranks (each rank runs its own batch: weak scaling)
+  ideal     = every tensor the op reads or writes, counted once
+  e2e       = the same metric with the inputs copied from pinned host memory
+              and every result copied back inside each timed step
+  roofline  = the dominant phase (the backward call) against the measured HBM
+              copy bandwidth; the forward kernel's own roofline beside it
+  images/s  = FlashInternImage-T core-op throughput: 64 images over the sum of
+              depth x step time of the four stages
+  cpu_baseline = the oracle (plain binary64 loops) on the host cores, on a
+              bounded sample of the same workload
+
+L2 is flushed (a write of twice its size) before every timed step, outside
+the step's events.  ``--impl reference`` times the oracle alone, on the host.
+Run under torchrun for N > 1 (one process per GPU).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from deformable_convolution_03_b300 import binding as B  # noqa: E402
+from deformable_convolution_03_b300.inputs import (  # noqa: E402
+    DTYPES, T_DEPTHS, WORKLOADS, Workload, ideal_bytes, make_inputs)
+
+METRIC = "DCN core fwd/bwd GB/s and % of HBM roofline; images/s at FlashInternImage-T shapes"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6400.0
+
+# DRAM traffic per launch from an ncu capture (profiles/), keyed by kernel and
+# workload, with the sha1 of the kernel source it was taken on: a changed
+# source voids the figure.
+TRAFFIC = {}
+
+
+def src_sha(name: str) -> str:
+    path = os.path.join(ROOT, "deformable_convolution_03_b300", "csrc", name)
+    return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+
+
+def traffic_for(key: str, src: str):
+    rec = TRAFFIC.get(key)
+    if not rec or rec["sha"] != src_sha(src):
+        return None
+    return rec["bytes"]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- clocks during the timed region (NVML reads only) ------------------------
+
+class ClockSampler:
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, index: int, period: float = 0.02):
+        self.index, self.period = index, period
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nv = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for k, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(k)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ---- one workload on the device ----------------------------------------------
+
+class Case:
+    """Device tensors, outputs and workspace of one workload."""
+
+    def __init__(self, w: Workload, dev):
+        self.w, self.dev = w, dev
+        t = make_inputs(w, grad=True)
+        self.host = t
+        self.p = B.Params(dtype=B.TORCH_TO_DCN[DTYPES[w.dtype]], **w.params())
+        self.x = {k: v.to(dev) for k, v in t.items()}
+        self.out = torch.empty(w.N, w.H_out, w.W_out, w.C, dtype=DTYPES[w.dtype], device=dev)
+        self.gi = torch.empty_like(self.x["input"])
+        self.go = torch.empty_like(self.x["offset"])
+        self.gm = torch.empty_like(self.x["mask"])
+        self.ws_bytes = B.dcn_core_bwd_workspace(self.p)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def fwd(self, x=None):
+        x = x or self.x
+        B.dcn_core_fwd(self.p, x["input"], x["offset"], x["mask"], self.out)
+
+    def bwd(self, x=None):
+        x = x or self.x
+        B.dcn_core_bwd(self.p, x["grad_out"], x["input"], x["offset"], x["mask"], self.gi,
+                       self.go, self.gm, self.ws, self.ws_bytes)
+
+    def launches_per_step(self) -> int:
+        # forward kernel; backward kernel; the rounding kernel of 16-bit grad_input
+        return 2 + (1 if self.ws_bytes else 0)
+
+
+def timed_steps(case: Case, steps: int, flush: torch.Tensor, phases=("fwd", "bwd")):
+    """Per-step, per-phase device times (ms), each step after an L2 flush."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+          for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        ev[k][0].record()
+        for j, ph in enumerate(phases):
+            getattr(case, ph)()
+            ev[k][j + 1].record()
+    torch.cuda.synchronize()
+    return {ph: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(steps)]
+            for j, ph in enumerate(phases)}
+
+
+def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
+    """The step through host buffers: pinned inputs in, every result out."""
+    hin = {k: v.pin_memory() for k, v in case.host.items()}
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            for t in (case.out, case.gi, case.go, case.gm)]
+    dev = {k: torch.empty_like(v) for k, v in case.x.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout)
+    times = []
+    for k in range(steps + 2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for key in dev:
+            dev[key].copy_(hin[key], non_blocking=True)
+        case.fwd(dev)
+        case.bwd(dev)
+        for h, d in zip(hout, (case.out, case.gi, case.go, case.gm)):
+            h.copy_(d, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if k >= 2:
+            times.append(a.elapsed_time(b))
+    return times, h2d, d2h
+
+
+def images_per_s(dev, flush, reps: int):
+    """FlashInternImage-T core op: 64 images / sum_i depth_i * t_i (fwd, fwd+bwd)."""
+    per_stage = []
+    for i, depth in enumerate(T_DEPTHS, start=1):
+        w = WORKLOADS[f"t_stage{i}_bf16"]
+        c = Case(w, dev)
+        for _ in range(3):
+            c.fwd()
+            c.bwd()
+        t = timed_steps(c, reps, flush)
+        per_stage.append((depth, statistics.median(t["fwd"]), statistics.median(t["bwd"])))
+        del c
+    fwd_s = sum(d * f for d, f, _ in per_stage) / 1e3
+    step_s = sum(d * (f + b) for d, f, b in per_stage) / 1e3
+    return {"fwd": 64 / fwd_s, "fwd_bwd": 64 / step_s,
+            "stages_ms": [{"depth": d, "fwd": round(f, 5), "bwd": round(b, 5)}
+                          for d, f, b in per_stage]}
+
+
+# ---- the oracle on the host --------------------------------------------------
+
+class OracleTimer:
+    """The oracle's forward + backward on a seeded random sample of output
+    pixels of the workload (all of their groups, points and channels).  The
+    throughput is scaled to the metric's unit by the fraction of output pixels
+    processed: ideal bytes x (sample / all pixels) / time."""
+
+    def __init__(self, w: Workload):
+        import numpy as np
+        import oracle
+        oracle.build()
+        self.o, self.w = oracle, w
+        t = make_inputs(w, grad=True)
+        self.f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+        self.q = oracle.Params(coord_f32=1, **w.params())
+        self.total = w.N * w.H_out * w.W_out
+        self.perm = np.random.default_rng(1234).permutation(self.total)
+        ib = ideal_bytes(w)
+        self.step_bytes = ib["fwd"] + ib["bwd"]
+        self.cores = oracle.max_threads()
+
+    def run(self, npix: int) -> float:
+        pix = self.perm[:npix]
+        f = self.f
+        t0 = time.perf_counter()
+        self.o.forward_pixels(self.q, f["input"], f["offset"], f["mask"], pix)
+        self.o.backward_pixels(self.q, f["grad_out"], f["input"], f["offset"], f["mask"], pix)
+        return time.perf_counter() - t0
+
+    def size_for(self, seconds: float) -> int:
+        n = min(self.total, 64)
+        dt = self.run(n)
+        while dt < 0.2 and n < self.total:
+            n = min(self.total, n * 4)
+            dt = self.run(n)
+        return int(max(16, min(self.total, n * seconds / max(dt, 1e-6))))
+
+    def gbs(self, npix: int, seconds: float) -> float:
+        return self.step_bytes * npix / self.total / seconds / 1e9
+
+    def describe(self, npix: int, seconds: float) -> str:
+        return (f"forward+backward of {npix} random output pixels of {self.total} "
+                f"({100.0 * npix / self.total:.2f}% of {self.w.name}) in {seconds:.2f} s, "
+                f"{self.cores} threads")
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle on the host cores, same metric and workload;
+    each step a bounded sample sized so that all steps end within minutes."""
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    ot = OracleTimer(w)
+    per_step = max(0.01, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
+    npix = ot.size_for(per_step)
+    times = []
+    for k in range(args.warmup + args.steps):
+        dt = ot.run(npix)
+        if k >= args.warmup:
+            times.append(dt)
+    total_t = sum(times)
+    value = ot.gbs(npix * len(times), total_t)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ot.step_bytes / (value * 1e9) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(w, args.gpus),
+        "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": ot.cores,
+                         "kind": "oracle",
+                         "sample": "each step: " + ot.describe(npix, total_t / len(times))},
+        "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: Workload, n: int) -> dict:
+    return {"workload": w.name,
+            "shape": f"N={w.N} H=W={w.H} C={w.C} G={w.G} gc={w.gc} k{w.kernel_h}x{w.kernel_w} "
+                     f"s{w.stride_h} p{w.pad_h} d{w.dilation_h} P={w.P}",
+            "op": "DCNv3 (softmax)" if w.softmax else "DCNv4 (raw mask)",
+            "step": "forward + backward (grad_input, grad_offset, grad_mask)",
+            "storage": w.dtype, "accumulate": "f32",
+            "global_batch": w.N * n, "per_gpu_batch": w.N, "parallelism": f"replicas x{n}",
+            "inputs": f"input U(-1,1), offsets N(0,{w.offset_std}) px, mask N(0,1), grad N(0,1)",
+            "l2": "flushed before every timed step (write of 2x L2)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="t_stage1_f16")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--no-stages", action="store_true", help="skip the T-stage images/s sweep")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=8.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    w = WORKLOADS[args.workload]
+    case = Case(w, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        case.fwd()
+        case.bwd()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    wall0 = time.perf_counter()
+    with ClockSampler(dev.index) as clk:
+        t = timed_steps(case, args.steps, flush)
+    barrier()
+    wall = time.perf_counter() - wall0
+
+    fwd_ms = statistics.mean(t["fwd"])
+    bwd_ms = statistics.mean(t["bwd"])
+    step_ms = fwd_ms + bwd_ms
+    if dist is not None:
+        v = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        step_ms, fwd_ms, bwd_ms = v.tolist()
+
+    ib = ideal_bytes(w)
+    step_bytes = ib["fwd"] + ib["bwd"]
+    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+
+    # end to end through host buffers
+    e2e_t, h2d, d2h = e2e_steps(case, args.e2e_steps, flush)
+    e2e_ms = statistics.median(e2e_t)
+    if dist is not None:
+        v = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        e2e_ms = v.item()
+    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    peak, peak_kind = hbm_peak()
+    fwd_gbs = ib["fwd"] / (fwd_ms * 1e-3) / 1e9
+    bwd_gbs = ib["bwd"] / (bwd_ms * 1e-3) / 1e9
+    dominant = "bwd" if bwd_ms >= fwd_ms else "fwd"
+    roof = {
+        "bwd": {"bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(bwd_gbs / peak, 4),
+                "traffic": traffic_for(f"bwd@{w.name}", "dcn_bwd.cu"),
+                "phase": "dcn_core_bwd: workspace memset + bwd_kernel + round_kernel",
+                "ms": round(bwd_ms, 5), "peak_source": f"{peak_kind} HBM copy bandwidth"},
+        "fwd": {"bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(fwd_gbs / peak, 4),
+                "traffic": traffic_for(f"fwd@{w.name}", "dcn_fwd.cu"),
+                "phase": "dcn_core_fwd: fwd_kernel", "ms": round(fwd_ms, 5),
+                "peak_source": f"{peak_kind} HBM copy bandwidth"},
+    }
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(w, world),
+        "roofline": {**roof[dominant], "kernel": dominant},
+        "roofline_fwd": roof["fwd"],
+        "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
+                      "fwd_median": round(statistics.median(t["fwd"]), 5),
+                      "bwd_median": round(statistics.median(t["bwd"]), 5)},
+        "ideal_bytes": {"fwd": ib["fwd"], "bwd": ib["bwd"]},
+        "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps * case.launches_per_step(),
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_stages:
+        line["images_per_s"] = images_per_s(dev, flush, reps=200)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        ot = OracleTimer(w)
+        npix = ot.size_for(args.cpu_budget)
+        dt = ot.run(npix)
+        line["cpu_baseline"] = {"value": round(ot.gbs(npix, dt), 5), "unit": UNIT,
+                                "cores": ot.cores, "kind": "oracle",
+                                "sample": ot.describe(npix, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,249 @@
+"""ctypes binding of libdcn_b300.so (include/dcn_core.h).
+
+Argument marshalling only: torch tensors become device pointers, the current
+torch stream becomes the cudaStream_t, and a non-zero dcn_status_t becomes a
+:class:`DCNError`.  Every step of the computation runs in the CUDA library;
+there is no other implementation behind these functions.  If the library has
+not been built, the first call raises.
+
+The functions named like the C entry points (``dcn_core_fwd`` ...) take
+caller-allocated tensors, exactly like the C ABI.  :func:`core_fwd` and
+:func:`core_bwd` allocate their results with torch first and then call those.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, fields
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdcn_b300.so")
+
+DCN_F32, DCN_F16, DCN_BF16 = 0, 1, 2
+DCN_OK = 0
+DCN_ERR_NULL, DCN_ERR_SHAPE, DCN_ERR_DTYPE, DCN_ERR_ALIGN = 1, 2, 3, 4
+DCN_ERR_UNSUPPORTED, DCN_ERR_CUDA, DCN_ERR_INTERNAL, DCN_ERR_WORKSPACE = 5, 6, 7, 8
+DCN_MAX_POINTS = 64
+
+TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: DCN_BF16}
+
+# Every symbol include/dcn_core.h declares.
+EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_bwd_workspace",
+           "dcn_core_bwd", "dcn_status_str", "dcn_version")
+
+
+class DCNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dcn_status_str(status)} (status {status})")
+
+
+class dcn_params_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "N", "H", "W", "G", "gc", "kernel_h", "kernel_w", "stride_h", "stride_w",
+        "pad_h", "pad_w", "dilation_h", "dilation_w")] + [
+        ("offset_scale", ctypes.c_float), ("softmax", ctypes.c_int),
+        ("remove_center", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+@dataclass
+class Params:
+    """Python mirror of dcn_params_t."""
+    N: int
+    H: int
+    W: int
+    G: int
+    gc: int
+    kernel_h: int = 3
+    kernel_w: int = 3
+    stride_h: int = 1
+    stride_w: int = 1
+    pad_h: int = 1
+    pad_w: int = 1
+    dilation_h: int = 1
+    dilation_w: int = 1
+    offset_scale: float = 1.0
+    softmax: int = 0
+    remove_center: int = 0
+    dtype: int = DCN_F32
+
+    def c(self) -> dcn_params_t:
+        return dcn_params_t(**{f.name: getattr(self, f.name) for f in fields(self)})
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with deformable_convolution_03_b300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        PP = ctypes.POINTER(dcn_params_t)
+        vp, ip = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
+        L.dcn_out_shape.argtypes = [PP, ip, ip]
+        L.dcn_num_points.argtypes = [PP]
+        L.dcn_core_fwd.argtypes = [PP, vp, vp, vp, vp, vp]
+        L.dcn_core_bwd_workspace.argtypes = [PP]
+        L.dcn_core_bwd_workspace.restype = ctypes.c_size_t
+        L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.dcn_status_str.argtypes = [ctypes.c_int]
+        L.dcn_status_str.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr() if x.numel() else None
+    return int(x)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DCN_OK:
+        raise DCNError(rc, where)
+
+
+def dcn_status_str(status: int) -> str:
+    return lib().dcn_status_str(int(status)).decode()
+
+
+def dcn_version() -> int:
+    return int(lib().dcn_version())
+
+
+def dcn_out_shape(p: Params) -> tuple[int, int]:
+    ho, wo = ctypes.c_int(), ctypes.c_int()
+    _check(lib().dcn_out_shape(ctypes.byref(p.c()), ctypes.byref(ho), ctypes.byref(wo)),
+           "dcn_out_shape")
+    return ho.value, wo.value
+
+
+def dcn_num_points(p: Params) -> int:
+    r = lib().dcn_num_points(ctypes.byref(p.c()))
+    if r < 0:
+        raise DCNError(-r, "dcn_num_points")
+    return r
+
+
+def dcn_core_fwd(p: Params, input, offset, mask, output, stream=None) -> None:
+    """Raw entry point: pointers (tensors or ints) in, output written in place."""
+    _check(lib().dcn_core_fwd(ctypes.byref(p.c()), _ptr(input), _ptr(offset), _ptr(mask),
+                              _ptr(output), _stream(stream)), "dcn_core_fwd")
+
+
+def dcn_core_bwd_workspace(p: Params) -> int:
+    return int(lib().dcn_core_bwd_workspace(ctypes.byref(p.c())))
+
+
+def dcn_core_bwd(p: Params, grad_out, input, offset, mask, grad_input, grad_offset, grad_mask,
+                 workspace=None, workspace_bytes: int | None = None, stream=None) -> None:
+    """Raw entry point: all three gradients written in place."""
+    if workspace_bytes is None:
+        workspace_bytes = (workspace.numel() * workspace.element_size()
+                           if isinstance(workspace, torch.Tensor) else 0)
+    _check(lib().dcn_core_bwd(ctypes.byref(p.c()), _ptr(grad_out), _ptr(input), _ptr(offset),
+                              _ptr(mask), _ptr(grad_input), _ptr(grad_offset), _ptr(grad_mask),
+                              _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "dcn_core_bwd")
+
+
+# ---- tensor-level convenience: shapes from the tensors, results allocated ----
+
+def params_for(input: torch.Tensor, G: int, **geom) -> Params:
+    """Params for a channels-last input tensor (N, H, W, G*gc) and G groups."""
+    if input.dim() != 4:
+        raise ValueError("input must be (N, H, W, G*gc)")
+    N, H, W, C = input.shape
+    if C % G:
+        raise ValueError(f"channels {C} not divisible by groups {G}")
+    if input.dtype not in TORCH_TO_DCN:
+        raise TypeError(f"unsupported dtype {input.dtype}")
+    return Params(N=N, H=H, W=W, G=G, gc=C // G, dtype=TORCH_TO_DCN[input.dtype], **geom)
+
+
+def _expect(t: torch.Tensor, name: str, shape: tuple, dtype, device) -> None:
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def shapes(p: Params) -> dict:
+    ho, wo = dcn_out_shape(p)
+    P = dcn_num_points(p)
+    C = p.G * p.gc
+    return {"input": (p.N, p.H, p.W, C), "offset": (p.N, ho, wo, p.G, P, 2),
+            "mask": (p.N, ho, wo, p.G, P), "output": (p.N, ho, wo, C)}
+
+
+def core_fwd(input, offset, mask, G: int, stream=None, out=None, **geom) -> torch.Tensor:
+    """output = the core op on CUDA tensors; geom: kernel_h ... remove_center."""
+    p = params_for(input, G, **geom)
+    sh = shapes(p)
+    if input.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for name, t in (("input", input), ("offset", offset), ("mask", mask)):
+        _expect(t, name, sh[name], input.dtype, input.device)
+    if out is None:
+        out = torch.empty(sh["output"], dtype=input.dtype, device=input.device)
+    _expect(out, "out", sh["output"], input.dtype, input.device)
+    dcn_core_fwd(p, input, offset, mask, out, stream)
+    return out
+
+
+def core_bwd(grad_out, input, offset, mask, G: int, stream=None, **geom):
+    """(grad_input, grad_offset, grad_mask) on CUDA tensors."""
+    p = params_for(input, G, **geom)
+    sh = shapes(p)
+    if input.device.type != "cuda":
+        raise ValueError("tensors must be on a CUDA device")
+    for name, t in (("input", input), ("offset", offset), ("mask", mask)):
+        _expect(t, name, sh[name], input.dtype, input.device)
+    _expect(grad_out, "grad_out", sh["output"], input.dtype, input.device)
+    gi = torch.empty_like(input)
+    go = torch.empty_like(offset)
+    gm = torch.empty_like(mask)
+    nbytes = dcn_core_bwd_workspace(p)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=input.device) if nbytes else None
+    dcn_core_bwd(p, grad_out, input, offset, mask, gi, go, gm, ws, nbytes, stream)
+    return gi, go, gm
+
+
+class DCNCoreFunction(torch.autograd.Function):
+    """autograd wrapper: forward and backward both run the CUDA library."""
+
+    @staticmethod
+    def forward(ctx, input, offset, mask, G, geom):
+        ctx.save_for_backward(input, offset, mask)
+        ctx.G, ctx.geom = G, geom
+        return core_fwd(input, offset, mask, G, **geom)
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        input, offset, mask = ctx.saved_tensors
+        gi, go, gm = core_bwd(grad_out.contiguous(), input, offset, mask, ctx.G, **ctx.geom)
+        return gi, go, gm, None, None
+
+
+def dcn_core(input, offset, mask, G: int, **geom) -> torch.Tensor:
+    """Differentiable core op (DCNv3 with softmax=1, DCNv4 with softmax=0)."""
+    return DCNCoreFunction.apply(input, offset, mask, G, geom)

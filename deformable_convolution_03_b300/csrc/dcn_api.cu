@@ -1,0 +1,241 @@
+// dcn_api.cu -- the C ABI of libdcn_b300 (declared in include/dcn_core.h):
+// argument validation, the choice of kernel instance, and the launches.
+//
+// Every check runs on the host before the first CUDA call, so a rejected
+// call leaves the device untouched.  No entry point allocates memory.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/dcn_core.h"
+#include "dcn_kernels.h"
+
+namespace {
+
+int elem_size(int dtype) {
+  switch (dtype) {
+    case DCN_F32: return 4;
+    case DCN_F16: return 2;
+    case DCN_BF16: return 2;
+    default: return 0;
+  }
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Largest coordinate magnitude for which integer pixel positions stay exact
+// in binary32 with room to spare.
+constexpr long long kMaxExtent = 1LL << 22;
+
+struct Geometry {
+  int Ho, Wo, P;
+  long long n_in, n_out, units;  // elements of input/output, (pixel, group) pairs
+};
+
+int validate(const dcn_params_t* p, Geometry* g) {
+  if (!p) return DCN_ERR_NULL;
+  if (elem_size(p->dtype) == 0) return DCN_ERR_DTYPE;
+  if (p->N < 0 || p->H < 1 || p->W < 1 || p->G < 1 || p->gc < 1) return DCN_ERR_SHAPE;
+  if (p->kernel_h < 1 || p->kernel_w < 1 || p->stride_h < 1 || p->stride_w < 1 ||
+      p->dilation_h < 1 || p->dilation_w < 1 || p->pad_h < 0 || p->pad_w < 0)
+    return DCN_ERR_SHAPE;
+  if (p->remove_center != 0 && p->remove_center != 1) return DCN_ERR_SHAPE;
+  if (p->softmax != 0 && p->softmax != 1) return DCN_ERR_SHAPE;
+  if (p->remove_center && (p->kernel_h % 2 == 0 || p->kernel_w % 2 == 0)) return DCN_ERR_SHAPE;
+  if (!std::isfinite(p->offset_scale)) return DCN_ERR_SHAPE;
+  const long long kk = (long long)p->kernel_h * p->kernel_w;
+  const long long P = kk - p->remove_center;
+  if (P > DCN_MAX_POINTS) return DCN_ERR_UNSUPPORTED;
+  const long long C = (long long)p->G * p->gc;
+  if (C > DCN_MAX_CHANNELS) return DCN_ERR_UNSUPPORTED;
+  const long long Hp = (long long)p->H + 2LL * p->pad_h, Wp = (long long)p->W + 2LL * p->pad_w;
+  const long long eh = (long long)p->dilation_h * (p->kernel_h - 1) + 1;
+  const long long ew = (long long)p->dilation_w * (p->kernel_w - 1) + 1;
+  if (Hp > kMaxExtent || Wp > kMaxExtent || eh > kMaxExtent || ew > kMaxExtent)
+    return DCN_ERR_UNSUPPORTED;
+  if (Hp < eh || Wp < ew) return DCN_ERR_SHAPE;
+  const long long Ho = (Hp - eh) / p->stride_h + 1, Wo = (Wp - ew) / p->stride_w + 1;
+  g->Ho = (int)Ho;
+  g->Wo = (int)Wo;
+  g->P = (int)P;
+  // element counts must fit comfortably in 62 bits
+  const long long lim = 1LL << 62;
+  const long long hw = (long long)p->H * p->W;
+  if (p->N > 0 && (hw > lim / p->N / C || Ho * Wo > lim / p->N / C / (2 * P)))
+    return DCN_ERR_UNSUPPORTED;
+  g->n_in = (long long)p->N * hw * C;
+  g->n_out = (long long)p->N * Ho * Wo * C;
+  g->units = (long long)p->N * Ho * Wo * p->G;
+  return DCN_OK;
+}
+
+void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
+  std::memset(kp, 0, sizeof *kp);
+  kp->N = p->N; kp->H = p->H; kp->W = p->W; kp->G = p->G; kp->gc = p->gc; kp->C = p->G * p->gc;
+  kp->Ho = g.Ho; kp->Wo = g.Wo; kp->P = g.P;
+  kp->stride_h = p->stride_h; kp->stride_w = p->stride_w;
+  kp->pad_h = p->pad_h; kp->pad_w = p->pad_w;
+  kp->cen_h = p->dilation_h * (p->kernel_h - 1) / 2;
+  kp->cen_w = p->dilation_w * (p->kernel_w - 1) / 2;
+  kp->offset_scale = p->offset_scale;
+  kp->softmax = p->softmax;
+  kp->units = g.units;
+  // x-major point order: the kernel column outer, the row inner; the centre
+  // tap deleted in place when asked.
+  int k = 0;
+  for (int ix = 0; ix < p->kernel_w; ++ix)
+    for (int iy = 0; iy < p->kernel_h; ++iy) {
+      if (p->remove_center && ix == (p->kernel_w - 1) / 2 && iy == (p->kernel_h - 1) / 2) continue;
+      kp->tap_x[k] = (float)(ix * p->dilation_w - kp->cen_w);
+      kp->tap_y[k] = (float)(iy * p->dilation_h - kp->cen_h);
+      ++k;
+    }
+}
+
+// Host-side fault hook for tests of the error path: with DCN_FAULT_INJECT=launch
+// in the environment a valid call reports DCN_ERR_CUDA instead of launching.
+bool fault_injected() {
+  const char* v = std::getenv("DCN_FAULT_INJECT");
+  return v && std::strcmp(v, "launch") == 0;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+// Channels per thread of the forward: the widest power of two dividing gc,
+// up to one 16-byte vector (or DCN_FWD_CPT), whose slices start aligned in
+// both the input and the output.
+int pick_fwd_cpt(const dcn_params_t* p, const void* in, const void* out) {
+  const int es = elem_size(p->dtype);
+  int cap = env_int("DCN_FWD_CPT", 16 / es);
+  for (int c = 32; c >= 1; c >>= 1) {
+    if (c > cap || p->gc % c) continue;
+    const size_t a = (size_t)(c * es < 16 ? c * es : 16);
+    if (aligned(in, a) && aligned(out, a)) return c;
+  }
+  return 1;
+}
+
+// Channels per thread of the backward: as the forward, and gc/c must be a
+// power of two no larger than 32 so that a unit's threads share a warp; 0
+// selects the kernel that takes any gc.
+int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const void* acc) {
+  const int es = elem_size(p->dtype);
+  int cap = env_int("DCN_BWD_CPT", 16 / es);
+  for (int c = 32; c >= 1; c >>= 1) {
+    if (c > cap || p->gc % c) continue;
+    const int chunks = p->gc / c;
+    if (chunks > 32 || (chunks & (chunks - 1))) continue;
+    const size_t a = (size_t)(c * es < 16 ? c * es : 16);
+    const size_t af = c % 4 == 0 ? 16 : (c % 2 == 0 ? 8 : 4);
+    if (aligned(in, a) && aligned(gout, a) && aligned(acc, af)) return c;
+  }
+  return 0;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCN_OK : DCN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int dcn_out_shape(const dcn_params_t* p, int* H_out, int* W_out) {
+  if (!H_out || !W_out) return DCN_ERR_NULL;
+  Geometry g;
+  int rc = validate(p, &g);
+  if (rc != DCN_OK) return rc;
+  *H_out = g.Ho;
+  *W_out = g.Wo;
+  return DCN_OK;
+}
+
+int dcn_num_points(const dcn_params_t* p) {
+  Geometry g;
+  int rc = validate(p, &g);
+  return rc != DCN_OK ? -rc : g.P;
+}
+
+int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
+                 void* output, void* stream) {
+  Geometry g;
+  int rc = validate(p, &g);
+  if (rc != DCN_OK) return rc;
+  if (g.units == 0) return DCN_OK;
+  if (!input || !offset || !mask || !output) return DCN_ERR_NULL;
+  const size_t es = (size_t)elem_size(p->dtype);
+  if (!aligned(input, es) || !aligned(mask, es) || !aligned(output, es) ||
+      !aligned(offset, 2 * es))
+    return DCN_ERR_ALIGN;
+  dcn::KParams kp;
+  fill_kparams(p, g, &kp);
+  const int cpt = pick_fwd_cpt(p, input, output);
+  if (fault_injected()) return DCN_ERR_CUDA;
+  return cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t dcn_core_bwd_workspace(const dcn_params_t* p) {
+  Geometry g;
+  if (validate(p, &g) != DCN_OK) return 0;
+  return p->dtype == DCN_F32 ? 0 : (size_t)g.n_in * sizeof(float);
+}
+
+int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
+                 const void* offset, const void* mask, void* grad_input, void* grad_offset,
+                 void* grad_mask, void* workspace, size_t workspace_bytes, void* stream) {
+  Geometry g;
+  int rc = validate(p, &g);
+  if (rc != DCN_OK) return rc;
+  if (g.units == 0) return DCN_OK;
+  if (!grad_out || !input || !offset || !mask || !grad_input || !grad_offset || !grad_mask)
+    return DCN_ERR_NULL;
+  const size_t es = (size_t)elem_size(p->dtype);
+  if (!aligned(grad_out, es) || !aligned(input, es) || !aligned(mask, es) ||
+      !aligned(offset, 2 * es) || !aligned(grad_input, es) || !aligned(grad_offset, es) ||
+      !aligned(grad_mask, es))
+    return DCN_ERR_ALIGN;
+  float* acc;
+  const size_t acc_bytes = (size_t)g.n_in * sizeof(float);
+  if (p->dtype == DCN_F32) {
+    acc = static_cast<float*>(grad_input);
+  } else {
+    if (!workspace || workspace_bytes < acc_bytes) return DCN_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return DCN_ERR_ALIGN;
+    acc = static_cast<float*>(workspace);
+  }
+  dcn::KParams kp;
+  fill_kparams(p, g, &kp);
+  const int cpt = pick_bwd_cpt(p, input, grad_out, acc);
+  if (fault_injected()) return DCN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g.n_in > 0) {
+    cudaError_t e = cudaMemsetAsync(acc, 0, acc_bytes, s);
+    if (e != cudaSuccess) return DCN_ERR_CUDA;
+  }
+  return cuda_status(dcn::launch_bwd(kp, p->dtype, cpt, grad_out, input, offset, mask, acc,
+                                     grad_input, grad_offset, grad_mask, s));
+}
+
+const char* dcn_status_str(int status) {
+  switch (status) {
+    case DCN_OK: return "DCN_OK";
+    case DCN_ERR_NULL: return "DCN_ERR_NULL: a required pointer is NULL";
+    case DCN_ERR_SHAPE: return "DCN_ERR_SHAPE: a size or geometry parameter is out of range";
+    case DCN_ERR_DTYPE: return "DCN_ERR_DTYPE: unknown dtype";
+    case DCN_ERR_ALIGN: return "DCN_ERR_ALIGN: a pointer is misaligned for its element type";
+    case DCN_ERR_UNSUPPORTED: return "DCN_ERR_UNSUPPORTED: outside the limits of this build";
+    case DCN_ERR_CUDA: return "DCN_ERR_CUDA: a CUDA call or kernel launch failed";
+    case DCN_ERR_INTERNAL: return "DCN_ERR_INTERNAL: internal consistency check failed";
+    case DCN_ERR_WORKSPACE: return "DCN_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown dcn status";
+  }
+}
+
+int dcn_version(void) { return 100; }
+
+}  // extern "C"

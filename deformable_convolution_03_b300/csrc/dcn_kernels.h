@@ -1,0 +1,24 @@
+// dcn_kernels.h -- launchers of the forward and backward kernels, called by
+// the C ABI layer (dcn_api.cu) after it has validated every argument.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "dcn_common.cuh"
+
+namespace dcn {
+
+// cpt: channels per thread (1, 2, 4, 8, 16 or 32; a divisor of gc whose slice
+// of every tensor row starts cpt*sizeof(T)-aligned).
+cudaError_t launch_fwd(const KParams& kp, int dtype, int cpt, const void* in, const void* off,
+                       const void* msk, void* out, cudaStream_t s);
+
+// cpt as above with gc/cpt a power of two no larger than 32, or 0 for the
+// one-thread-per-unit kernel that takes any gc.  gin_acc: the float32
+// accumulator (zeroed by the caller); when it is not gin itself, a rounding
+// kernel writes gin from it afterwards.
+cudaError_t launch_bwd(const KParams& kp, int dtype, int cpt, const void* gout, const void* in,
+                       const void* off, const void* msk, float* gin_acc, void* gin, void* goff,
+                       void* gmask, cudaStream_t s);
+
+}  // namespace dcn

@@ -1,0 +1,136 @@
+/*
+ * dcn_core.h -- C ABI of the B300 (sm_103a) DCNv3 / DCNv4 core deformable
+ * aggregation library (libdcn_b300.so).
+ *
+ * The operation.  For every output pixel (n, ho, wo), group g and sampling
+ * point p the op forms a location from the receptive-field reference point,
+ * the dilation grid scaled by offset_scale and the predicted offset scaled by
+ * offset_scale; samples the zero-padded channels-last input there bilinearly
+ * (grid_sample's align_corners=False, padding_mode=zeros conventions); weights
+ * the sampled group vector by the point's modulation weight; and sums over the
+ * points.  This is dcnv3_core_pytorch as walked through on the page
+ * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读",
+ * section 四 steps 1-5.  The weights are a softmax over the points of each
+ * (pixel, group) for DCNv3 (same page, section 三 item 3) and the raw mask
+ * for DCNv4 (page "DCNv4高效实践指南：掌握可变形卷积的3倍速度提升技术",
+ * section 核心架构与性能优化).
+ *
+ * In unpadded pixel units, with c_w = floor(dilation_w*(kernel_w-1)/2) and
+ * tap t_x = ix*dilation_w - c_w (ix the kernel column):
+ *     x = fma(dx, offset_scale, fma(t_x, offset_scale, wo*stride_w - pad_w + c_w))
+ * evaluated in binary32, and likewise for y.  Corners outside [0,W)x[0,H)
+ * read zero.  A sample whose x is not in (-1, W) or y not in (-1, H) (this
+ * includes NaN and infinite offsets) contributes nothing and gets no gradient.
+ *
+ * Tensors (all channels-last, contiguous, one dtype per call, device memory):
+ *     input      (N, H, W, G*gc)
+ *     offset     (N, H_out, W_out, G, P, 2)   (dx, dy) in pixels
+ *     mask       (N, H_out, W_out, G, P)      logits if softmax, else weights
+ *     output     (N, H_out, W_out, G*gc)
+ * P = kernel_h*kernel_w - remove_center.  The P points are ordered x-major:
+ * p = ix*kernel_h + iy over kernel column ix and row iy, with the centre
+ * deleted in place when remove_center is set.
+ *
+ * Precision.  Storage in float32, float16 or bfloat16; all arithmetic in
+ * float32 (fp32 accumulation over points and channels); results rounded to the
+ * storage dtype to nearest-even.
+ *
+ * Ownership and streams.  Every tensor pointer is caller-owned device memory;
+ * the library never allocates, frees or retains memory.  Work is enqueued on
+ * the caller's cudaStream_t (NULL: the legacy default stream) and the call
+ * returns without synchronising: a DCN_OK return covers argument checks and
+ * launch errors only.  Calls are safe from several host threads on different
+ * streams.  Inputs must not alias outputs.
+ *
+ * Errors.  Every entry point returns a dcn_status_t (int) and never prints,
+ * throws or aborts.  Argument checks run on the host before any CUDA call, so
+ * an invalid call has no effect on the device.
+ */
+#ifndef DCN_CORE_H
+#define DCN_CORE_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { DCN_F32 = 0, DCN_F16 = 1, DCN_BF16 = 2 } dcn_dtype_t;
+
+typedef enum {
+  DCN_OK = 0,
+  DCN_ERR_NULL = 1,        /* a required pointer is NULL */
+  DCN_ERR_SHAPE = 2,       /* a size or geometry parameter is out of range */
+  DCN_ERR_DTYPE = 3,       /* dtype is not a dcn_dtype_t */
+  DCN_ERR_ALIGN = 4,       /* a tensor pointer is not aligned to its element size */
+  DCN_ERR_UNSUPPORTED = 5, /* valid but not supported by this build (see limits) */
+  DCN_ERR_CUDA = 6,        /* a CUDA runtime call or kernel launch failed */
+  DCN_ERR_INTERNAL = 7,    /* internal consistency check failed */
+  DCN_ERR_WORKSPACE = 8    /* workspace missing or smaller than dcn_core_bwd_workspace() */
+} dcn_status_t;
+
+/* Limits of this build. */
+#define DCN_MAX_POINTS 64          /* P = kernel_h*kernel_w - remove_center */
+#define DCN_MAX_CHANNELS 65536     /* G*gc */
+
+typedef struct {
+  int N, H, W;               /* batch and input spatial size, N >= 0, H, W >= 1 */
+  int G, gc;                 /* groups and channels per group, >= 1 */
+  int kernel_h, kernel_w;    /* >= 1; both odd when remove_center */
+  int stride_h, stride_w;    /* >= 1 */
+  int pad_h, pad_w;          /* >= 0; pad_h pads the height, pad_w the width */
+  int dilation_h, dilation_w;/* >= 1 */
+  float offset_scale;        /* scales both the dilation grid and the offsets */
+  int softmax;               /* 1: DCNv3, the mask holds logits; 0: DCNv4 raw weights */
+  int remove_center;         /* 1: the centre tap is not sampled */
+  int dtype;                 /* dcn_dtype_t of every tensor of the call */
+} dcn_params_t;
+
+/* Output size: H_out = (H + 2*pad_h - (dilation_h*(kernel_h-1)+1)) / stride_h + 1
+ * (integer division), likewise W_out; the size a strided, dilated convolution
+ * gives (section 四 step 1 of the walkthrough).  Host only.
+ * DCN_ERR_NULL / DCN_ERR_SHAPE / DCN_ERR_DTYPE on bad arguments. */
+int dcn_out_shape(const dcn_params_t* p, int* H_out, int* W_out);
+
+/* P, the number of sampling points per (pixel, group), or a negative
+ * dcn_status_t on bad arguments.  Host only. */
+int dcn_num_points(const dcn_params_t* p);
+
+/* Forward: output = sum_p m_p * bilinear(input, location_p)   (steps 1-5).
+ * input, offset, mask: read; output: fully overwritten.  N == 0 launches
+ * nothing.  stream: a cudaStream_t. */
+int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset,
+                 const void* mask, void* output, void* stream);
+
+/* Bytes of device workspace dcn_core_bwd needs: N*H*W*G*gc*4 (a float32
+ * accumulator for grad_input) for float16 / bfloat16, 0 for float32.
+ * Returns 0 as well when the parameters are invalid. */
+size_t dcn_core_bwd_workspace(const dcn_params_t* p);
+
+/* Backward of L = <grad_out, output>: the analytic derivative of the forward.
+ *   grad_input  (N, H, W, G*gc)          dL/d input, fully overwritten
+ *   grad_offset (N, H_out, W_out, G, P, 2)  dL/d offset, fully overwritten
+ *   grad_mask   (N, H_out, W_out, G, P)  dL/d mask; with softmax this is the
+ *                                        gradient with respect to the logits
+ * At an integer location the cell [x0, x0+1] is used, so the offset gradient
+ * there is the one-sided derivative from the right.  grad_input is formed by
+ * float32 atomic additions, so its rounding (not its value) depends on the
+ * order the GPU runs them in.  workspace: caller-owned device memory of at
+ * least dcn_core_bwd_workspace(p) bytes, 16-byte aligned (may be NULL when
+ * that is 0); its contents on entry do not matter and on return are
+ * unspecified. */
+int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
+                 const void* offset, const void* mask, void* grad_input, void* grad_offset,
+                 void* grad_mask, void* workspace, size_t workspace_bytes, void* stream);
+
+/* A static, human-readable name for a dcn_status_t. */
+const char* dcn_status_str(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int dcn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCN_CORE_H */

@@ -82,6 +82,8 @@ def _load():
         lib.dcno_forward_pixels.argtypes = [P, D, D, D, ctypes.POINTER(ctypes.c_longlong),
                                             ctypes.c_long, D]
         lib.dcno_backward.argtypes = [P, D, D, D, D, D, D, D]
+        lib.dcno_backward_pixels.argtypes = [P, D, D, D, D, ctypes.POINTER(ctypes.c_longlong),
+                                             ctypes.c_long, D, D, D]
         lib.dcno_set_threads.argtypes = [ctypes.c_int]
         lib.dcno_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -164,6 +166,22 @@ def backward(p: Params, grad_out, input, offset, mask):
     if _load().dcno_backward(ctypes.byref(p._c()), _dp(grad_out), _dp(input), _dp(offset),
                              _dp(mask), _dp(gi), _dp(go), _dp(gm)):
         raise ValueError("oracle backward rejected the parameters")
+    return gi, go, gm
+
+
+def backward_pixels(p: Params, grad_out, input, offset, mask, pixels):
+    """Backward restricted to flat output pixels: (grad_input from their scatter
+    only, grad_offset (len, G, P, 2), grad_mask (len, G, P))."""
+    ho, wo, P, C, input, offset, mask = _check(p, input, offset, mask)
+    grad_out = _f64(grad_out)
+    pix = np.ascontiguousarray(np.asarray(pixels, dtype=np.int64))
+    gi = np.zeros((p.N, p.H, p.W, C), dtype=np.float64)
+    go = np.zeros((pix.size, p.G, P, 2), dtype=np.float64)
+    gm = np.zeros((pix.size, p.G, P), dtype=np.float64)
+    if _load().dcno_backward_pixels(ctypes.byref(p._c()), _dp(grad_out), _dp(input), _dp(offset),
+                                    _dp(mask), pix.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)),
+                                    pix.size, _dp(gi), _dp(go), _dp(gm)):
+        raise ValueError("oracle backward_pixels rejected the arguments")
     return gi, go, gm
 
 

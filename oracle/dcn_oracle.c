@@ -265,6 +265,85 @@ int dcno_forward_pixels(const dcno_params* q, const double* input, const double*
 
 /* ---- backward ----------------------------------------------------------- */
 
+/* Gradients of L = <grad_out, output> contributed by one output pixel:
+ * grad_offset and grad_mask of its G*P points are written to goff_pix and
+ * gmask_pix; its scatter into grad_input is added to grad_input (atomically
+ * when several threads may add to the same element). */
+static void backward_pixel(const dcno_params* q, int Ho, int Wo, const int* tx, const int* ty,
+                           int P, const double* grad_out, const double* input,
+                           const double* offset, const double* mask, long pix,
+                           double* grad_input, double* goff_pix, double* gmask_pix, int atomic) {
+  int n = (int)(pix / ((long)Ho * Wo));
+  int ho = (int)((pix / Wo) % Ho);
+  int wo = (int)(pix % Wo);
+  long C = (long)q->G * q->gc;
+  int cw = (q->dilation_w * (q->kernel_w - 1)) / 2;
+  int ch = (q->dilation_h * (q->kernel_h - 1)) / 2;
+  double os = q->offset_scale;
+  double m[DCNO_MAX_P], gm[DCNO_MAX_P];
+  const double* go = grad_out + pix * C;
+  for (int g = 0; g < q->G; ++g) {
+    long unit = pix * q->G + g;
+    const double* off = offset + unit * P * 2;
+    double* goff = goff_pix + (long)g * P * 2;
+    weights(q, mask + unit * P, P, m);
+    for (int p = 0; p < P; ++p) {
+      double x = location(wo, q->stride_w, q->pad_w, cw, tx[p], off[2 * p + 0], os, q->coord_f32);
+      double y = location(ho, q->stride_h, q->pad_h, ch, ty[p], off[2 * p + 1], os, q->coord_f32);
+      dcno_cell cl = cell_of(q, x, y);
+      gm[p] = 0.0;
+      goff[2 * p + 0] = 0.0;
+      goff[2 * p + 1] = 0.0;
+      if (!cl.valid) continue;
+      double wx[2] = {1.0 - cl.fx, cl.fx}, wy[2] = {1.0 - cl.fy, cl.fy};
+      double dvdx = 0.0, dvdy = 0.0, dv = 0.0;
+      for (int cc = 0; cc < q->gc; ++cc) {
+        double gcc = go[(long)g * q->gc + cc];
+        double v[2][2];
+        for (int a = 0; a < 2; ++a)
+          for (int b = 0; b < 2; ++b) v[a][b] = corner(q, input, n, cl.y0 + a, cl.x0 + b, g, cc);
+        /* d sample / d pixel-x and / d pixel-y, inside the cell */
+        double sx = wy[0] * (v[0][1] - v[0][0]) + wy[1] * (v[1][1] - v[1][0]);
+        double sy = wx[0] * (v[1][0] - v[0][0]) + wx[1] * (v[1][1] - v[0][1]);
+        double s = wy[0] * (wx[0] * v[0][0] + wx[1] * v[0][1]) +
+                   wy[1] * (wx[0] * v[1][0] + wx[1] * v[1][1]);
+        dv += gcc * s;
+        dvdx += gcc * sx;
+        dvdy += gcc * sy;
+        /* scatter into the input: corners in the zero padding have no input
+         * element and receive nothing */
+        for (int a = 0; a < 2; ++a)
+          for (int b = 0; b < 2; ++b) {
+            long yy = cl.y0 + a, xx = cl.x0 + b;
+            if (yy < 0 || yy >= q->H || xx < 0 || xx >= q->W) continue;
+            double* dst =
+                &grad_input[(((long)n * q->H + yy) * q->W + xx) * C + (long)g * q->gc + cc];
+            double add = m[p] * wy[a] * wx[b] * gcc;
+            if (atomic) {
+#pragma omp atomic
+              *dst += add;
+            } else {
+              *dst += add;
+            }
+          }
+      }
+      gm[p] = dv;
+      /* the location moves by offset_scale per unit of offset */
+      goff[2 * p + 0] = os * m[p] * dvdx;
+      goff[2 * p + 1] = os * m[p] * dvdy;
+    }
+    double* gmask = gmask_pix + (long)g * P;
+    if (q->softmax) {
+      /* d softmax: g_logit_p = m_p * (g_m_p - sum_q m_q g_m_q) */
+      double dot = 0.0;
+      for (int p = 0; p < P; ++p) dot += m[p] * gm[p];
+      for (int p = 0; p < P; ++p) gmask[p] = m[p] * (gm[p] - dot);
+    } else {
+      for (int p = 0; p < P; ++p) gmask[p] = gm[p];
+    }
+  }
+}
+
 /* Gradients of L = <grad_out, output> with respect to input, offset and mask
  * (the mask logits when softmax is set).  All three outputs are overwritten.
  * Work is split by image n: every scatter into grad_input stays inside the
@@ -277,75 +356,37 @@ int dcno_backward(const dcno_params* q, const double* grad_out, const double* in
   if ((long)q->kernel_h * q->kernel_w > DCNO_MAX_P) return -1;
   int P = dcno_taps(q, tx, ty);
   long C = (long)q->G * q->gc;
-  int cw = (q->dilation_w * (q->kernel_w - 1)) / 2;
-  int ch = (q->dilation_h * (q->kernel_h - 1)) / 2;
-  double os = q->offset_scale;
   memset(grad_input, 0, sizeof(double) * (size_t)q->N * q->H * q->W * C);
-
 #pragma omp parallel for schedule(dynamic, 1)
-  for (int n = 0; n < q->N; ++n) {
-    double m[DCNO_MAX_P], gm[DCNO_MAX_P];
-    for (int ho = 0; ho < Ho; ++ho)
-      for (int wo = 0; wo < Wo; ++wo) {
-        long pix = ((long)n * Ho + ho) * Wo + wo;
-        const double* go = grad_out + pix * C;
-        for (int g = 0; g < q->G; ++g) {
-          long unit = pix * q->G + g;
-          const double* off = offset + unit * P * 2;
-          double* goff = grad_offset + unit * P * 2;
-          weights(q, mask + unit * P, P, m);
-          for (int p = 0; p < P; ++p) {
-            double x = location(wo, q->stride_w, q->pad_w, cw, tx[p], off[2 * p + 0], os,
-                                q->coord_f32);
-            double y = location(ho, q->stride_h, q->pad_h, ch, ty[p], off[2 * p + 1], os,
-                                q->coord_f32);
-            dcno_cell cl = cell_of(q, x, y);
-            gm[p] = 0.0;
-            goff[2 * p + 0] = 0.0;
-            goff[2 * p + 1] = 0.0;
-            if (!cl.valid) continue;
-            double wx[2] = {1.0 - cl.fx, cl.fx}, wy[2] = {1.0 - cl.fy, cl.fy};
-            double dvdx = 0.0, dvdy = 0.0, dv = 0.0;
-            for (int cc = 0; cc < q->gc; ++cc) {
-              double gcc = go[(long)g * q->gc + cc];
-              double v[2][2];
-              for (int a = 0; a < 2; ++a)
-                for (int b = 0; b < 2; ++b) v[a][b] = corner(q, input, n, cl.y0 + a, cl.x0 + b, g, cc);
-              /* d sample / d pixel-x and / d pixel-y, inside the cell */
-              double sx = wy[0] * (v[0][1] - v[0][0]) + wy[1] * (v[1][1] - v[1][0]);
-              double sy = wx[0] * (v[1][0] - v[0][0]) + wx[1] * (v[1][1] - v[0][1]);
-              double s = wy[0] * (wx[0] * v[0][0] + wx[1] * v[0][1]) +
-                         wy[1] * (wx[0] * v[1][0] + wx[1] * v[1][1]);
-              dv += gcc * s;
-              dvdx += gcc * sx;
-              dvdy += gcc * sy;
-              /* scatter into the input: corners in the zero padding have no
-               * input element and receive nothing */
-              for (int a = 0; a < 2; ++a)
-                for (int b = 0; b < 2; ++b) {
-                  long yy = cl.y0 + a, xx = cl.x0 + b;
-                  if (yy < 0 || yy >= q->H || xx < 0 || xx >= q->W) continue;
-                  grad_input[(((long)n * q->H + yy) * q->W + xx) * C + (long)g * q->gc + cc] +=
-                      m[p] * wy[a] * wx[b] * gcc;
-                }
-            }
-            gm[p] = dv;
-            /* the location moves by offset_scale per unit of offset */
-            goff[2 * p + 0] = os * m[p] * dvdx;
-            goff[2 * p + 1] = os * m[p] * dvdy;
-          }
-          double* gmask = grad_mask + unit * P;
-          if (q->softmax) {
-            /* d softmax: g_logit_p = m_p * (g_m_p - sum_q m_q g_m_q) */
-            double dot = 0.0;
-            for (int p = 0; p < P; ++p) dot += m[p] * gm[p];
-            for (int p = 0; p < P; ++p) gmask[p] = m[p] * (gm[p] - dot);
-          } else {
-            for (int p = 0; p < P; ++p) gmask[p] = gm[p];
-          }
-        }
-      }
-  }
+  for (int n = 0; n < q->N; ++n)
+    for (long r = 0; r < (long)Ho * Wo; ++r) {
+      long pix = (long)n * Ho * Wo + r;
+      backward_pixel(q, Ho, Wo, tx, ty, P, grad_out, input, offset, mask, pix, grad_input,
+                     grad_offset + pix * q->G * P * 2, grad_mask + pix * q->G * P, 0);
+    }
+  return 0;
+}
+
+/* The backward restricted to the listed output pixels (flat indices as in
+ * dcno_forward_pixels): grad_input (full size, overwritten) receives only their
+ * scatter; grad_offset and grad_mask receive G*P*2 and G*P values per listed
+ * pixel.  For timing on a bounded sample and for spot checks. */
+int dcno_backward_pixels(const dcno_params* q, const double* grad_out, const double* input,
+                         const double* offset, const double* mask, const long long* pixels,
+                         long npix, double* grad_input, double* grad_offset, double* grad_mask) {
+  int Ho, Wo, tx[DCNO_MAX_P], ty[DCNO_MAX_P];
+  if (dcno_out_shape(q, &Ho, &Wo) != 0) return -1;
+  if ((long)q->kernel_h * q->kernel_w > DCNO_MAX_P) return -1;
+  int P = dcno_taps(q, tx, ty);
+  long C = (long)q->G * q->gc;
+  long total = (long)q->N * Ho * Wo;
+  for (long i = 0; i < npix; ++i)
+    if (pixels[i] < 0 || pixels[i] >= total) return -1;
+  memset(grad_input, 0, sizeof(double) * (size_t)q->N * q->H * q->W * C);
+#pragma omp parallel for schedule(dynamic, 4)
+  for (long i = 0; i < npix; ++i)
+    backward_pixel(q, Ho, Wo, tx, ty, P, grad_out, input, offset, mask, (long)pixels[i],
+                   grad_input, grad_offset + i * q->G * P * 2, grad_mask + i * q->G * P, 1);
   return 0;
 }
 

@@ -17,3 +17,11 @@ def oracle_lib():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def native():
+    """The CUDA library's binding, with the library built in-tree."""
+    from deformable_convolution_03_b300 import build, binding
+    build.build()
+    return binding

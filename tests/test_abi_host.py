@@ -1,0 +1,167 @@
+"""The C ABI on the host: symbols, output geometry and every argument check.
+
+Nothing here launches a kernel.  Calls that would pass validation are made
+only with the host-side fault hook set (which reports DCN_ERR_CUDA before any
+CUDA call), and only where no GPU is present, so no fake pointer can ever
+reach a device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from deformable_convolution_03_b300.inputs import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# aligned fake device addresses; never dereferenced (every call that uses them
+# fails validation, or stops at the fault hook before any CUDA call)
+A = 1 << 20
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dcn_core.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(dcn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(native):
+    names = declared_functions()
+    assert set(names) == set(native.EXPORTS), names
+    lib = native.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert native.dcn_version() >= 100
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_out_shape_matches_workload_table(native, name):
+    w = WORKLOADS[name]
+    p = native.Params(dtype=native.DCN_F32, **w.params())
+    assert native.dcn_out_shape(p) == (w.H_out, w.W_out)
+    assert native.dcn_num_points(p) == w.P
+    assert native.dcn_core_bwd_workspace(p) == 0
+    p.dtype = native.DCN_BF16
+    assert native.dcn_core_bwd_workspace(p) == w.N * w.H * w.W * w.C * 4
+
+
+@pytest.mark.parametrize("geom", [
+    dict(kernel_h=1, kernel_w=1, pad_h=0, pad_w=0),
+    dict(kernel_h=5, kernel_w=3, pad_h=2, pad_w=0, stride_w=2),
+    dict(kernel_h=3, kernel_w=3, pad_h=0, pad_w=3, dilation_w=3),
+    dict(kernel_h=7, kernel_w=7, pad_h=3, pad_w=3, remove_center=1),
+    dict(stride_h=3, stride_w=2, dilation_h=2, pad_h=0),
+])
+def test_out_shape_matches_oracle(native, oracle_lib, geom):
+    for H, W in ((7, 6), (16, 9), (31, 31)):
+        p = native.Params(N=2, H=H, W=W, G=2, gc=4, **geom)
+        q = oracle_lib.Params(N=2, H=H, W=W, G=2, gc=4, **geom)
+        assert native.dcn_out_shape(p) == oracle_lib.out_shape(q)
+        assert native.dcn_num_points(p) == oracle_lib.num_points(q)
+
+
+BAD = [
+    (dict(dtype=3), "DCN_ERR_DTYPE"),
+    (dict(dtype=-1), "DCN_ERR_DTYPE"),
+    (dict(N=-1), "DCN_ERR_SHAPE"),
+    (dict(H=0), "DCN_ERR_SHAPE"),
+    (dict(W=0), "DCN_ERR_SHAPE"),
+    (dict(G=0), "DCN_ERR_SHAPE"),
+    (dict(gc=0), "DCN_ERR_SHAPE"),
+    (dict(kernel_h=0), "DCN_ERR_SHAPE"),
+    (dict(stride_w=0), "DCN_ERR_SHAPE"),
+    (dict(dilation_h=0), "DCN_ERR_SHAPE"),
+    (dict(pad_w=-1), "DCN_ERR_SHAPE"),
+    (dict(kernel_h=4, remove_center=1), "DCN_ERR_SHAPE"),
+    (dict(softmax=2), "DCN_ERR_SHAPE"),
+    (dict(offset_scale=float("nan")), "DCN_ERR_SHAPE"),
+    (dict(H=2, pad_h=0), "DCN_ERR_SHAPE"),                  # kernel larger than the image
+    (dict(kernel_h=9, kernel_w=9), "DCN_ERR_UNSUPPORTED"),   # 81 points
+    (dict(G=1024, gc=128), "DCN_ERR_UNSUPPORTED"),          # 131072 channels
+    (dict(H=1 << 23), "DCN_ERR_UNSUPPORTED"),
+]
+
+
+@pytest.mark.parametrize("bad,code", BAD)
+def test_invalid_parameters_rejected_by_every_entry(native, bad, code):
+    p = native.Params(**{**dict(N=1, H=8, W=8, G=2, gc=4), **bad})
+    want = getattr(native, code)
+    lib = native.lib()
+    ho, wo = ctypes.c_int(), ctypes.c_int()
+    assert lib.dcn_out_shape(ctypes.byref(p.c()), ctypes.byref(ho), ctypes.byref(wo)) == want
+    assert lib.dcn_num_points(ctypes.byref(p.c())) == -want
+    assert lib.dcn_core_fwd(ctypes.byref(p.c()), A, A, A, A, None) == want
+    assert lib.dcn_core_bwd(ctypes.byref(p.c()), A, A, A, A, A, A, A, A, 1 << 30, None) == want
+    assert lib.dcn_core_bwd_workspace(ctypes.byref(p.c())) == 0
+    assert code in native.dcn_status_str(want)
+
+
+def test_null_arguments(native):
+    lib = native.lib()
+    p = native.Params(N=1, H=8, W=8, G=2, gc=4)
+    assert lib.dcn_out_shape(None, None, None) == native.DCN_ERR_NULL
+    assert lib.dcn_out_shape(ctypes.byref(p.c()), None, None) == native.DCN_ERR_NULL
+    assert lib.dcn_core_fwd(None, A, A, A, A, None) == native.DCN_ERR_NULL
+    for i in range(4):
+        ptrs = [A] * 4
+        ptrs[i] = None
+        assert lib.dcn_core_fwd(ctypes.byref(p.c()), *ptrs, None) == native.DCN_ERR_NULL
+    for i in range(7):
+        ptrs = [A] * 7
+        ptrs[i] = None
+        assert lib.dcn_core_bwd(ctypes.byref(p.c()), *ptrs, None, 0, None) == native.DCN_ERR_NULL
+
+
+def test_misaligned_pointers(native):
+    lib = native.lib()
+    for dtype, es in ((native.DCN_F32, 4), (native.DCN_F16, 2), (native.DCN_BF16, 2)):
+        p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=dtype)
+        for i in range(4):
+            ptrs = [A] * 4
+            ptrs[i] = A + (es if i == 1 else 1)  # offset pairs need 2*elem alignment
+            assert lib.dcn_core_fwd(ctypes.byref(p.c()), *ptrs, None) == native.DCN_ERR_ALIGN
+        for i in range(7):
+            ptrs = [A] * 7
+            ptrs[i] = A + (es if i == 2 else 1)
+            assert lib.dcn_core_bwd(ctypes.byref(p.c()), *ptrs, A, 1 << 30,
+                                    None) == native.DCN_ERR_ALIGN
+        if dtype != native.DCN_F32:
+            assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([A] * 7), A + 8, 1 << 30,
+                                    None) == native.DCN_ERR_ALIGN
+
+
+def test_workspace_checks(native):
+    lib = native.lib()
+    p = native.Params(N=2, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)
+    need = native.dcn_core_bwd_workspace(p)
+    assert need == 2 * 8 * 8 * 8 * 4
+    assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([A] * 7), None, need,
+                            None) == native.DCN_ERR_WORKSPACE
+    assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([A] * 7), A, need - 4,
+                            None) == native.DCN_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(native):
+    lib = native.lib()
+    p = native.Params(N=0, H=8, W=8, G=2, gc=4)
+    assert lib.dcn_core_fwd(ctypes.byref(p.c()), None, None, None, None, None) == native.DCN_OK
+    assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([None] * 8), 0, None) == native.DCN_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers only where no GPU exists")
+def test_fault_hook_reports_cuda_error(native, monkeypatch):
+    lib = native.lib()
+    p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)
+    monkeypatch.setenv("DCN_FAULT_INJECT", "launch")
+    assert lib.dcn_core_fwd(ctypes.byref(p.c()), A, A, A, A, None) == native.DCN_ERR_CUDA
+    assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([A] * 8), 1 << 30, None) == native.DCN_ERR_CUDA
+    with pytest.raises(native.DCNError, match="DCN_ERR_CUDA"):
+        native.dcn_core_fwd(p, A, A, A, A, stream=0)
+
+
+def test_status_strings(native):
+    for code in range(9):
+        assert native.dcn_status_str(code).startswith("DCN_")
+    assert "unknown" in native.dcn_status_str(99)

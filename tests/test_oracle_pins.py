@@ -456,3 +456,30 @@ def test_coord_f32_mode_is_within_rounding_otherwise():
     mask = rng.normal(0, 1, (1, ho, wo, 2, P))
     a, b = oracle.forward(p32, x, off, mask), oracle.forward(p64, x, off, mask)
     assert np.max(np.abs(a - b)) < 1e-5
+
+
+# --------------------------------------------------------------------------
+# the pixel-list entry points agree with the whole-tensor ones
+
+def test_pixel_subsets_match_whole_tensor_results():
+    p = Params(N=2, H=6, W=5, G=2, gc=3, softmax=1, stride_h=2)
+    ho, wo, P = shapes(p)
+    rng = np.random.default_rng(16)
+    x = rng.uniform(-1, 1, (2, 6, 5, 6))
+    off = rng.normal(0, 2, (2, ho, wo, 2, P, 2))
+    mask = rng.normal(0, 1, (2, ho, wo, 2, P))
+    go = rng.normal(0, 1, (2, ho, wo, 6))
+    out = oracle.forward(p, x, off, mask)
+    gi, goff, gm = oracle.backward(p, go, x, off, mask)
+    allpix = np.arange(2 * ho * wo)
+    np.testing.assert_array_equal(oracle.forward_pixels(p, x, off, mask, allpix),
+                                  out.reshape(-1, 6))
+    gi2, goff2, gm2 = oracle.backward_pixels(p, go, x, off, mask, allpix)
+    np.testing.assert_allclose(gi2, gi, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(goff2, goff.reshape(-1, 2, P, 2))
+    np.testing.assert_array_equal(gm2, gm.reshape(-1, 2, P))
+    some = rng.choice(allpix, 7, replace=False)
+    np.testing.assert_array_equal(oracle.forward_pixels(p, x, off, mask, some),
+                                  out.reshape(-1, 6)[some])
+    _, goff3, gm3 = oracle.backward_pixels(p, go, x, off, mask, some)
+    np.testing.assert_array_equal(goff3, goff.reshape(-1, 2, P, 2)[some])
