@@ -222,6 +222,7 @@ static void forward_pixel(const dcno_params* q, int Ho, int Wo, const int* tx, c
       double y = location(ho, q->stride_h, q->pad_h, ch, ty[p], off[2 * p + 1], q->offset_scale,
                           q->coord_f32);
       dcno_cell cl = cell_of(q, x, y);
+      if (!cl.valid) continue; /* contributes nothing, whatever its weight */
       for (int cc = 0; cc < q->gc; ++cc)
         out_pix[(long)g * q->gc + cc] += m[p] * bilinear(q, input, n, &cl, g, cc);
     }
