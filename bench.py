@@ -75,50 +75,91 @@ def hbm_peak():
 # ---- clocks during the timed region (NVML reads only) ------------------------
 
 class ClockSampler:
+    """SM clock and throttle reasons of the benchmarked GPU, sampled in a
+    background thread while the timed steps run (reads only; the GPU is found
+    by UUID, so the index NVML uses does not matter).  Falls back to
+    nvidia-smi's query loop when NVML is unavailable."""
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    SMI = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+           "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+           "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, period: float = 0.02):
-        self.index, self.period = index, period
+    def __init__(self, dev, period: float = 0.02):
+        self.period = period
         self.samples, self.reasons = [], set()
-        self.max_mhz = None
+        self.max_mhz, self.error, self.nv, self.proc = None, None, None, None
         self._stop = threading.Event()
         self._t = None
+        self.uuid = None
+        try:
+            u = str(torch.cuda.get_device_properties(dev).uuid)
+            self.uuid = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception as e:  # pragma: no cover - depends on the torch build
+            self.error = f"uuid: {e}"
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
+            self.nv = pynvml
+        except Exception as e:
+            self.error = f"nvml: {e}"
 
     def _run(self):
+        get_reasons = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
         while not self._stop.is_set():
             try:
                 self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                r = get_reasons(self.h)
                 for k, bit in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(k)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = f"nvml sample: {e}"
             time.sleep(self.period)
 
     def __enter__(self):
         if self.nv is not None:
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
+        elif self.uuid:
+            import subprocess
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.SMI}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            # the first sample marks that the query loop is running
+            self.first = self.proc.stdout.readline()
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self._t is not None:
             self._t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            out, _ = self.proc.communicate()
+            out = getattr(self, "first", "") + out
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for row in out.splitlines():
+                f = [x.strip() for x in row.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, v in zip(names, f[2:]):
+                    if v.lower().startswith("active"):
+                        self.reasons.add(name)
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "error": self.error}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
@@ -354,7 +395,7 @@ def main():
 
     barrier()
     wall0 = time.perf_counter()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev) as clk:
         t = timed_steps(case, args.steps, flush)
     barrier()
     wall = time.perf_counter() - wall0
@@ -372,13 +413,17 @@ def main():
     value = world * step_bytes / (step_ms * 1e-3) / 1e9
 
     # end to end through host buffers
-    e2e_t, h2d, d2h = e2e_steps(case, args.e2e_steps, flush)
-    e2e_ms = statistics.median(e2e_t)
-    if dist is not None:
-        v = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        e2e_ms = v.item()
-    e2e_val = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e_t, h2d, d2h = e2e_steps(case, args.e2e_steps, flush)
+        e2e_ms = statistics.median(e2e_t)
+        if dist is not None:
+            v = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(v, op=dist.ReduceOp.MAX)
+            e2e_ms = v.item()
+        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 4)}
 
     peak, peak_kind = hbm_peak()
     fwd_gbs = ib["fwd"] / (fwd_ms * 1e-3) / 1e9
@@ -408,8 +453,7 @@ def main():
                       "fwd_median": round(statistics.median(t["fwd"]), 5),
                       "bwd_median": round(statistics.median(t["bwd"]), 5)},
         "ideal_bytes": {"fwd": ib["fwd"], "bwd": ib["bwd"]},
-        "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "e2e": e2e,
         "gpu_launches": args.steps * case.launches_per_step(),
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),

@@ -71,6 +71,17 @@ int validate(const dcn_params_t* p, Geometry* g) {
   return DCN_OK;
 }
 
+dcn::FastDiv fast_div(uint32_t d) {
+  // see dcn::FastDiv: s = ceil(log2 d), mul = floor(2^32 (2^s - d) / d) + 1
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  dcn::FastDiv f;
+  f.mul = (uint32_t)(((1ull << 32) * ((1ull << s) - d)) / d + 1);
+  f.shift = s;
+  f.d = d;
+  return f;
+}
+
 void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
   std::memset(kp, 0, sizeof *kp);
   kp->N = p->N; kp->H = p->H; kp->W = p->W; kp->G = p->G; kp->gc = p->gc; kp->C = p->G * p->gc;
@@ -82,6 +93,9 @@ void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
   kp->offset_scale = p->offset_scale;
   kp->softmax = p->softmax;
   kp->units = g.units;
+  kp->div_G = fast_div((uint32_t)p->G);
+  kp->div_Wo = fast_div((uint32_t)g.Wo);
+  kp->div_Ho = fast_div((uint32_t)g.Ho);
   // x-major point order: the kernel column outer, the row inner; the centre
   // tap deleted in place when asked.
   int k = 0;
@@ -107,11 +121,24 @@ int env_int(const char* name, int dflt) {
   return std::atoi(v);
 }
 
-// Channels per thread of the forward: the widest power of two dividing gc,
-// up to one 16-byte vector (or DCN_FWD_CPT), whose slices start aligned in
-// both the input and the output.
-int pick_fwd_cpt(const dcn_params_t* p, const void* in, const void* out) {
+// Channels per thread of the forward.  The wide kernel (returned negated)
+// takes slices of 16 channels (or 8, 4) of 16 to 64 bytes when the unit count
+// and every image's element count fit in 31 bits and the input and output are
+// 32-byte aligned (16 for a 16-byte slice).  Otherwise the general kernel with
+// the widest power of two dividing gc up to one 16-byte vector (or
+// DCN_FWD_CPT), whose slices start aligned in both the input and the output.
+int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const void* out) {
   const int es = elem_size(p->dtype);
+  const long long img = (long long)p->H * p->W * p->G * p->gc;
+  if (env_int("DCN_FWD_WIDE", 1) && img < (1LL << 31)) {
+    for (int c = 16; c >= 4; c >>= 1) {
+      const int bytes = c * es;
+      if (p->gc % c || bytes < 16 || bytes > 64) continue;
+      if (g.units * (p->gc / c) >= (1LL << 31)) continue;
+      const size_t a = bytes >= 32 ? 32 : 16;
+      if (aligned(in, a) && aligned(out, a)) return -c;
+    }
+  }
   int cap = env_int("DCN_FWD_CPT", 16 / es);
   for (int c = 32; c >= 1; c >>= 1) {
     if (c > cap || p->gc % c) continue;
@@ -173,7 +200,7 @@ int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, c
     return DCN_ERR_ALIGN;
   dcn::KParams kp;
   fill_kparams(p, g, &kp);
-  const int cpt = pick_fwd_cpt(p, input, output);
+  const int cpt = pick_fwd_cpt(p, g, input, output);
   if (fault_injected()) return DCN_ERR_CUDA;
   return cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
                                      static_cast<cudaStream_t>(stream)));

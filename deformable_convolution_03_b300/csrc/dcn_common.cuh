@@ -12,6 +12,18 @@
 
 namespace dcn {
 
+// Unsigned division by a runtime-invariant divisor d as a multiply and a shift
+// (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up variant): with s = ceil(log2 d) and
+// mul = floor(2^32 (2^s - d) / d) + 1, n / d = (umulhi(n, mul) + n) >> s for
+// every n < 2^31 (the sum stays below 2^32).
+struct FastDiv {
+  uint32_t mul, shift, d;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    return (__umulhi(n, mul) + n) >> shift;
+  }
+};
+
 // Everything a kernel needs about one call, passed by value (kernel parameter
 // space, so warp-uniform reads of it are cheap).
 struct KParams {
@@ -23,6 +35,7 @@ struct KParams {
   float offset_scale;
   int softmax;
   long long units;           // N*Ho*Wo*G: one (pixel, group) pair each
+  FastDiv div_G, div_Wo, div_Ho;
   // Kernel taps of the P points, in point order (x-major, centre removed when
   // asked): ix*dilation_w - cen_w and iy*dilation_h - cen_h, as floats (exact).
   float tap_x[DCN_MAX_POINTS];
@@ -133,6 +146,81 @@ struct Slice {
     }
   }
 };
+
+// ---- wide gathers: NW 32-bit words from a 32-byte-aligned address -----------
+
+template <int NW>
+__device__ __forceinline__ void ldg_words(const void* p, uint32_t (&w)[NW]) {
+  static_assert(NW % 4 == 0, "16-byte multiples only");
+  const char* c = static_cast<const char*>(p);
+  if constexpr (NW % 8 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW / 8; ++i)
+      asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+          : "=r"(w[8 * i + 0]), "=r"(w[8 * i + 1]), "=r"(w[8 * i + 2]), "=r"(w[8 * i + 3]),
+            "=r"(w[8 * i + 4]), "=r"(w[8 * i + 5]), "=r"(w[8 * i + 6]), "=r"(w[8 * i + 7])
+          : "l"(c + 32 * i));
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW / 4; ++i) {
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(c) + i);
+      w[4 * i + 0] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
+    }
+  }
+}
+
+// acc[0..2*NW) += weight * (the 16-bit or 32-bit elements packed in w), one
+// product per element, accumulated in float32.  16-bit storage: the weight is
+// rounded to the storage type once and each product is exact in float32
+// (mixed-precision fma.rn.f32.{f16,bf16}); float32 storage: paired f32x2 FMAs.
+template <typename T> struct Fma;
+
+template <> struct Fma<__half> {
+  using W = unsigned short;
+  __device__ __forceinline__ static W weight(float w) {
+    return __half_as_ushort(__float2half_rn(w));
+  }
+  __device__ __forceinline__ static void word(float& a0, float& a1, uint32_t v, W w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "fma.rn.f32.f16 %0, lo, %3, %0;\n\tfma.rn.f32.f16 %1, hi, %3, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(v), "h"(w));
+  }
+};
+
+template <> struct Fma<__nv_bfloat16> {
+  using W = unsigned short;
+  __device__ __forceinline__ static W weight(float w) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(w));
+  }
+  __device__ __forceinline__ static void word(float& a0, float& a1, uint32_t v, W w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, lo, %3, %0;\n\tfma.rn.f32.bf16 %1, hi, %3, %1;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(v), "h"(w));
+  }
+};
+
+template <> struct Fma<float> {
+  using W = float;
+  __device__ __forceinline__ static W weight(float w) { return w; }
+  // two consecutive float32 elements (words v0, v1) in one f32x2 FMA
+  __device__ __forceinline__ static void pair(float& a0, float& a1, uint32_t v0, uint32_t v1,
+                                              float w) {
+    asm("{\n\t.reg .b64 a, c, s;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 c, {%2, %3};\n\t"
+        "mov.b64 s, {%4, %4};\n\tfma.rn.f32x2 a, c, s, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1) : "r"(v0), "r"(v1), "f"(w));
+  }
+};
+
+template <typename T, int NW>
+__device__ __forceinline__ void fma_words(float* acc, const uint32_t (&v)[NW], typename Fma<T>::W w) {
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) Fma<T>::word(acc[2 * i], acc[2 * i + 1], v[i], w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < NW; i += 2) Fma<T>::pair(acc[i], acc[i + 1], v[i], v[i + 1], w);
+  }
+}
 
 // ---- the sampling location of one point (binary32, fused multiply-adds) ------
 // ref = o*stride - pad + cen (unpadded pixel units, exact in binary32);

@@ -106,10 +106,102 @@ fwd_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ 
   Slice<T, CPT>::store(output + unit * kp.gc + c0, acc);
 }
 
+// The wide kernel: one thread per (unit, slice of CPT channels) where a
+// slice is 16, 32 or 64 bytes and every corner is one or two 256-bit loads.
+// Corners outside the image keep a valid (clamped) address and get weight 0,
+// so every thread runs the same straight-line code for every point.  Needs
+// the unit count and each image's element count below 2^31.
+template <typename T, int CPT, int KP>
+__global__ void __launch_bounds__(256)
+fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ offset,
+                const T* __restrict__ mask, T* __restrict__ output) {
+  constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words per corner
+  const int chunks = kp.gc / CPT;
+  const uint32_t item = blockIdx.x * blockDim.x + threadIdx.x;
+  if (item >= (uint32_t)(kp.units * chunks)) return;
+  const uint32_t unit = chunks == 1 ? item : item / (uint32_t)chunks;
+  const int c0 = (int)(item - unit * chunks) * CPT;
+  const uint32_t q1 = kp.div_G.div(unit);
+  const int g = (int)(unit - q1 * (uint32_t)kp.G);
+  const uint32_t q2 = kp.div_Wo.div(q1);
+  const int wo = (int)(q1 - q2 * (uint32_t)kp.Wo);
+  const uint32_t n = kp.div_Ho.div(q2);
+  const int ho = (int)(q2 - n * (uint32_t)kp.Ho);
+
+  const int P = KP > 0 ? KP : kp.P;
+  const T* mrow = mask + (size_t)unit * P;
+  const T* orow = offset + (size_t)unit * P * 2;
+  const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
+  const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
+  const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
+  const float ref_y = (float)(ho * kp.stride_h - kp.pad_h + kp.cen_h);
+  const float scale = kp.offset_scale;
+
+  // DCNv3: softmax statistics of the unit's logits
+  float mx = 0.f, inv = 1.f;
+  if (kp.softmax) {
+    mx = -INFINITY;
+    for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
+    float s = 0.f;
+    for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
+    inv = 1.f / s;
+  }
+
+  float acc[CPT];
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) acc[i] = 0.f;
+
+#pragma unroll(KP > 0 ? KP : 3)
+  for (int p = 0; p < P; ++p) {
+    float m = Dt<T>::one(mrow + p);
+    if (kp.softmax) m = expf(m - mx) * inv;
+    const float2 d = Dt<T>::two(orow + 2 * p);
+    float x = location(d.x, kp.tap_x[p], scale, ref_x);
+    float y = location(d.y, kp.tap_y[p], scale, ref_y);
+    if (!in_box(x, y, kp.W, kp.H)) {  // also NaN / inf: every corner falls outside
+      x = -4.f;
+      y = -4.f;
+    }
+    const float xf = floorf(x), yf = floorf(y);
+    const int x0 = (int)xf, y0 = (int)yf;
+    const float fx = x - xf, fy = y - yf;
+    const float wy0 = (uint32_t)y0 < H ? (1.f - fy) * m : 0.f;
+    const float wy1 = (uint32_t)(y0 + 1) < H ? fy * m : 0.f;
+    const float wx0 = (uint32_t)x0 < W ? 1.f - fx : 0.f;
+    const float wx1 = (uint32_t)(x0 + 1) < W ? fx : 0.f;
+    // clamped corners: always inside the image, weight 0 when really outside
+    const uint32_t xa = min((uint32_t)x0, W - 1), xb = min((uint32_t)(x0 + 1), W - 1);
+    const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
+    const uint32_t ra = ya * WC, rb = yb * WC, ca = xa * C, cb = xb * C;
+    uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
+    ldg_words<NW>(img + (ra + ca), v00);
+    ldg_words<NW>(img + (ra + cb), v01);
+    ldg_words<NW>(img + (rb + ca), v10);
+    ldg_words<NW>(img + (rb + cb), v11);
+    fma_words<T, NW>(acc, v00, Fma<T>::weight(wy0 * wx0));
+    fma_words<T, NW>(acc, v01, Fma<T>::weight(wy0 * wx1));
+    fma_words<T, NW>(acc, v10, Fma<T>::weight(wy1 * wx0));
+    fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1 * wx1));
+  }
+  Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
+}
+
+template <typename T, int CPT>
+static void launch_wide(const KParams& kp, unsigned grid, int block, cudaStream_t s, const T* i_,
+                        const T* o_, const T* m_, T* y_) {
+  constexpr int bytes = CPT * (int)sizeof(T);
+  if constexpr (bytes >= 16 && bytes <= 64) {
+    if (kp.P == 9)
+      fwd_wide_kernel<T, CPT, 9><<<grid, block, 0, s>>>(kp, i_, o_, m_, y_);
+    else
+      fwd_wide_kernel<T, CPT, 0><<<grid, block, 0, s>>>(kp, i_, o_, m_, y_);
+  }
+}
+
 template <typename T>
 static cudaError_t launch_fwd_t(const KParams& kp, int cpt, const void* in, const void* off,
                                 const void* msk, void* out, cudaStream_t s) {
-  const long long items = kp.units * (kp.gc / cpt);
+  const long long items = kp.units * (kp.gc / (cpt < 0 ? -cpt : cpt));
   const int block = 256;
   const long long grid = (items + block - 1) / block;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
@@ -122,6 +214,9 @@ static cudaError_t launch_fwd_t(const KParams& kp, int cpt, const void* in, cons
     case K: fwd_kernel<T, K><<<(unsigned)grid, block, 0, s>>>(kp, i_, o_, m_, y_); break;
     DCN_CASE(1) DCN_CASE(2) DCN_CASE(4) DCN_CASE(8) DCN_CASE(16) DCN_CASE(32)
 #undef DCN_CASE
+    case -4: launch_wide<T, 4>(kp, (unsigned)grid, block, s, i_, o_, m_, y_); break;
+    case -8: launch_wide<T, 8>(kp, (unsigned)grid, block, s, i_, o_, m_, y_); break;
+    case -16: launch_wide<T, 16>(kp, (unsigned)grid, block, s, i_, o_, m_, y_); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

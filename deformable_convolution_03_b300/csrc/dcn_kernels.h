@@ -9,7 +9,9 @@
 namespace dcn {
 
 // cpt: channels per thread (1, 2, 4, 8, 16 or 32; a divisor of gc whose slice
-// of every tensor row starts cpt*sizeof(T)-aligned).
+// of every tensor row starts cpt*sizeof(T)-aligned) for the general kernel;
+// -cpt (cpt*sizeof(T) of 16, 32 or 64 bytes, slices 32-byte aligned when 32 or
+// more) selects the wide kernel.
 cudaError_t launch_fwd(const KParams& kp, int dtype, int cpt, const void* in, const void* off,
                        const void* msk, void* out, cudaStream_t s);
 

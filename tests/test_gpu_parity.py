@@ -91,14 +91,24 @@ def test_small_forward_and_backward(w):
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("cap", [1, 2, 4, 8, 16, 32])
-def test_every_kernel_instance(dt, cap, monkeypatch):
-    # force each channels-per-thread instance of both kernels
+def test_every_general_kernel_instance(dt, cap, monkeypatch):
+    # force each channels-per-thread instance of the general kernels
+    monkeypatch.setenv("DCN_FWD_WIDE", "0")
     monkeypatch.setenv("DCN_FWD_CPT", str(cap))
     monkeypatch.setenv("DCN_BWD_CPT", str(cap))
     w = small(f"inst_{dt}_{cap}", dt, gc=32, G=2, softmax=1, N=3, H=10, W=9)
     t = make_inputs(w)
     check_fwd(w, t)
     check_bwd(w, t)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("gc", [4, 8, 16, 24, 48])
+@pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
+def test_wide_forward_instances(dt, gc, sm, rc):
+    # slices of 4, 8 and 16 channels, 9 points and the runtime point count
+    w = small(f"wide_{dt}_{gc}", dt, gc=gc, G=3, softmax=sm, remove_center=rc, N=2, H=11, W=13)
+    check_fwd(w, make_inputs(w))
 
 
 # ---- hand-worked cases and exact identities -----------------------------------
