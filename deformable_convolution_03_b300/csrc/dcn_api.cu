@@ -131,7 +131,9 @@ int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const
   const int es = elem_size(p->dtype);
   const long long img = (long long)p->H * p->W * p->G * p->gc;
   if (env_int("DCN_FWD_WIDE", 1) && img < (1LL << 31)) {
+    const int wcap = env_int("DCN_FWD_WIDE_CPT", 16);
     for (int c = 16; c >= 4; c >>= 1) {
+      if (c > wcap) continue;
       const int bytes = c * es;
       if (p->gc % c || bytes < 16 || bytes > 64) continue;
       if (g.units * (p->gc / c) >= (1LL << 31)) continue;
@@ -148,12 +150,15 @@ int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const
   return 1;
 }
 
-// Channels per thread of the backward: as the forward, and gc/c must be a
-// power of two no larger than 32 so that a unit's threads share a warp; 0
-// selects the kernel that takes any gc.
+// Channels per thread of the backward: a power of two dividing gc, at most 4
+// (or DCN_BWD_CPT), with gc/c a power of two no larger than 32 so that a
+// unit's threads are adjacent lanes of one warp; 0 selects the kernel that
+// takes any gc.  Four float32 channels per lane make the lanes of one unit
+// cover whole 32-byte sectors of grad_input in a single vector reduction,
+// which halves the L2 reduction requests against one lane per 16 channels.
 int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const void* acc) {
   const int es = elem_size(p->dtype);
-  int cap = env_int("DCN_BWD_CPT", 16 / es);
+  int cap = env_int("DCN_BWD_CPT", 4);
   for (int c = 32; c >= 1; c >>= 1) {
     if (c > cap || p->gc % c) continue;
     const int chunks = p->gc / c;
