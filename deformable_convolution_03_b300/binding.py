@@ -31,7 +31,8 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_bwd_workspace",
-           "dcn_core_bwd", "dcn_status_str", "dcn_version")
+           "dcn_core_bwd", "dcn_core_bwd_noalloc", "dcn_status_str", "dcn_version")
+DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class DCNError(RuntimeError):
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
         L.dcn_core_bwd_workspace.argtypes = [PP]
         L.dcn_core_bwd_workspace.restype = ctypes.c_size_t
         L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -160,6 +162,19 @@ def dcn_core_bwd(p: Params, grad_out, input, offset, mask, grad_input, grad_offs
                               _ptr(mask), _ptr(grad_input), _ptr(grad_offset), _ptr(grad_mask),
                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "dcn_core_bwd")
+
+
+def dcn_core_bwd_noalloc(p: Params, grad_out, input, offset, mask, grad_input, grad_offset,
+                         grad_mask, stream=None) -> None:
+    """The backward without a workspace: for callers that may not allocate
+    device memory where they run it.  The float32 accumulator that float16 /
+    bfloat16 need comes from the library's own static device array
+    (DCN_NOALLOC_SCRATCH_BYTES), shared by all calls on a device, so calls
+    must not overlap on the GPU."""
+    _check(lib().dcn_core_bwd_noalloc(ctypes.byref(p.c()), _ptr(grad_out), _ptr(input),
+                                      _ptr(offset), _ptr(mask), _ptr(grad_input),
+                                      _ptr(grad_offset), _ptr(grad_mask), _stream(stream)),
+           "dcn_core_bwd_noalloc")
 
 
 # ---- tensor-level convenience: shapes from the tensors, results allocated ----

@@ -123,6 +123,42 @@ int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
                  const void* offset, const void* mask, void* grad_input, void* grad_offset,
                  void* grad_mask, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library's own device scratch array used by
+ * dcn_core_bwd_noalloc: 32 MiB, enough for the float32 grad_input accumulator
+ * of 8M input elements (N*H*W*G*gc <= 8388608). */
+#define DCN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* The backward for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this entry point exists for deployment, not for the method.
+ *
+ * Some callers are not allowed to allocate at the point where they run the
+ * backward: a plugin inside another runtime that owns all device memory and
+ * hands out none during execution, or code with a fixed memory budget that
+ * must not grow after start-up (a cudaMalloc there would also synchronise the
+ * device).  Such callers cannot provide the workspace dcn_core_bwd needs for
+ * float16 / bfloat16.  This entry point computes exactly what dcn_core_bwd
+ * computes, with the same arguments minus the workspace, and takes its
+ * float32 accumulator from a static array inside the library
+ * (DCN_NOALLOC_SCRATCH_BYTES per GPU that loads the library, held until the
+ * process exits).  It allocates nothing and calls no allocating routine.
+ *
+ *   - Requests whose dcn_core_bwd_workspace(p) exceeds
+ *     DCN_NOALLOC_SCRATCH_BYTES return DCN_ERR_UNSUPPORTED before any CUDA
+ *     call; other argument errors are those of dcn_core_bwd.
+ *   - The first call on a device (that needs the array: float16 / bfloat16)
+ *     looks up the array's device address on the current device, once; make
+ *     that first call before any stream capture.  The stream must belong to
+ *     the current device.
+ *   - All calls on a device share the one array.  Each call clears what it
+ *     uses before use, but two calls whose work overlaps on the GPU (different
+ *     streams, no ordering between them) race on it and give wrong results:
+ *     order them, or use dcn_core_bwd with separate workspaces.
+ *   - float32 needs no scratch; the call then behaves as dcn_core_bwd with no
+ *     workspace. */
+int dcn_core_bwd_noalloc(const dcn_params_t* p, const void* grad_out, const void* input,
+                         const void* offset, const void* mask, void* grad_input,
+                         void* grad_offset, void* grad_mask, void* stream);
+
 /* A static, human-readable name for a dcn_status_t. */
 const char* dcn_status_str(int status);
 
