@@ -49,7 +49,12 @@ FALLBACK_HBM_GBS = 6400.0
 # DRAM traffic per launch from an ncu capture (profiles/), keyed by kernel and
 # workload, with the sha1 of the kernel source it was taken on: a changed
 # source voids the figure.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/fwd_wide_t_stage1_f16.md
+    "fwd@t_stage1_f16": {"bytes": 69_075_200 + 6_083_328, "sha": "44766e2214a2"},
+    # profiles/bwd_kernel_t_stage1_f16.md: bwd_kernel + round_kernel (the memset is not a kernel)
+    "bwd@t_stage1_f16": {"bytes": 146_137_088 + 48_210_432 + 51_387_136 + 1_556_736, "sha": "09a7ce77d4d5"},
+}
 
 
 def src_sha(name: str) -> str:
