@@ -314,6 +314,24 @@ static cudaError_t launch_bwd_t(const KParams& kp, int cpt, const void* gout, co
   return e;
 }
 
+cudaError_t launch_round(int dtype, const float* acc, void* out, long long n, cudaStream_t s) {
+  const int block = 256;
+  long long rg = (n + block - 1) / block;
+  if (rg > 148LL * 64) rg = 148LL * 64;
+  if (rg <= 0) return cudaSuccess;
+  switch (dtype) {
+    case DCN_F16:
+      round_kernel<__half><<<(unsigned)rg, block, 0, s>>>(acc, static_cast<__half*>(out), n);
+      break;
+    case DCN_BF16:
+      round_kernel<__nv_bfloat16><<<(unsigned)rg, block, 0, s>>>(
+          acc, static_cast<__nv_bfloat16*>(out), n);
+      break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd(const KParams& kp, int dtype, int cpt, const void* gout, const void* in,
                        const void* off, const void* msk, float* gin_acc, void* gin, void* goff,
                        void* gmask, cudaStream_t s) {

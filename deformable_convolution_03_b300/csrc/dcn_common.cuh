@@ -42,6 +42,26 @@ struct KParams {
   float tap_y[DCN_MAX_POINTS];
 };
 
+// Geometry of the windowed backward (bwd_window_kernel): a CTA owns TH x TW
+// output pixels of one (image, group) and a window of WH x WW input pixels
+// whose origin, for the tile starting at output (ho0, wo0), is
+// (ho0*stride_h + org_y, wo0*stride_w + org_x).
+struct WinGeom {
+  int TH, TW;
+  int tiles_h, tiles_w;
+  int WH, WW;
+  int org_y, org_x;
+};
+
+// Shared memory of bwd_window_kernel: TH*TW*P sample entries in cell order
+// (16 B each), the tile's grad_out (gc*es bytes per output pixel), and
+// per-cell counts, list heads and cursors ((WH-1)*(WW-1) cells).
+__host__ __device__ inline size_t window_smem_bytes(const WinGeom& wg, int P, int gc, int es) {
+  const size_t nunit = (size_t)wg.TH * wg.TW, nsamp = nunit * P;
+  const size_t ncell = (size_t)(wg.WH - 1) * (wg.WW - 1);
+  return nsamp * 16 + nunit * gc * es + (3 * ncell + 1) * sizeof(int);
+}
+
 // ---- storage dtype traits ---------------------------------------------------
 
 template <typename T> struct Dt;
@@ -210,6 +230,26 @@ template <> struct Fma<float> {
         : "+f"(a0), "+f"(a1) : "r"(v0), "r"(v1), "f"(w));
   }
 };
+
+// s0 += lo(v) * lo(g), s1 += hi(v) * hi(g): the dot product of two packed
+// 16-bit pairs, each product exact in float32.
+template <typename T>
+__device__ __forceinline__ void dot_word(float& s0, float& s1, uint32_t v, uint32_t g);
+
+template <>
+__device__ __forceinline__ void dot_word<__half>(float& s0, float& s1, uint32_t v, uint32_t g) {
+  asm("{\n\t.reg .b16 vl, vh, gl, gh;\n\tmov.b32 {vl, vh}, %2;\n\tmov.b32 {gl, gh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, vl, gl, %0;\n\tfma.rn.f32.f16 %1, vh, gh, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(v), "r"(g));
+}
+
+template <>
+__device__ __forceinline__ void dot_word<__nv_bfloat16>(float& s0, float& s1, uint32_t v,
+                                                        uint32_t g) {
+  asm("{\n\t.reg .b16 vl, vh, gl, gh;\n\tmov.b32 {vl, vh}, %2;\n\tmov.b32 {gl, gh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, vl, gl, %0;\n\tfma.rn.f32.bf16 %1, vh, gh, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(v), "r"(g));
+}
 
 template <typename T, int NW>
 __device__ __forceinline__ void fma_words(float* acc, const uint32_t (&v)[NW], typename Fma<T>::W w) {

@@ -23,4 +23,15 @@ cudaError_t launch_bwd(const KParams& kp, int dtype, int cpt, const void* gout, 
                        const void* off, const void* msk, float* gin_acc, void* gin, void* goff,
                        void* gmask, cudaStream_t s);
 
+// float32 accumulator -> 16-bit grad_input (n elements), rounding to nearest.
+cudaError_t launch_round(int dtype, const float* acc, void* out, long long n, cudaStream_t s);
+
+// The windowed backward (dcn_bwd_window.cu): cpt 4, 8 or 16 with cpt*sizeof(T)
+// of 16 to 64 bytes, gc/cpt a power of two no larger than 32, P <= 16; 256
+// threads per CTA = TH*TW*(gc/cpt).  gin_acc (float32) must be cleared by the
+// caller; when it is not gin, it is rounded into gin at the end.
+cudaError_t launch_bwd_window(const KParams& kp, const WinGeom& wg, int dtype, int cpt,
+                              const void* gout, const void* in, const void* off, const void* msk,
+                              float* gin_acc, void* gin, void* goff, void* gmask, cudaStream_t s);
+
 }  // namespace dcn

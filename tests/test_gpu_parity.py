@@ -94,6 +94,7 @@ def test_small_forward_and_backward(w):
 def test_every_general_kernel_instance(dt, cap, monkeypatch):
     # force each channels-per-thread instance of the general kernels
     monkeypatch.setenv("DCN_FWD_WIDE", "0")
+    monkeypatch.setenv("DCN_BWD_WINDOW", "0")
     monkeypatch.setenv("DCN_FWD_CPT", str(cap))
     monkeypatch.setenv("DCN_BWD_CPT", str(cap))
     w = small(f"inst_{dt}_{cap}", dt, gc=32, G=2, softmax=1, N=3, H=10, W=9)
@@ -109,6 +110,58 @@ def test_wide_forward_instances(dt, gc, sm, rc):
     # slices of 4, 8 and 16 channels, 9 points and the runtime point count
     w = small(f"wide_{dt}_{gc}", dt, gc=gc, G=3, softmax=sm, remove_center=rc, N=2, H=11, W=13)
     check_fwd(w, make_inputs(w))
+
+
+SPLIT = [
+    small("sp_f16_g16", "f16", gc=16, G=4, N=2, H=21, W=19),
+    small("sp_f32_far", "f32", gc=16, G=2, N=2, H=20, W=23, offset_std=7.0),
+    small("sp_bf16_s2d2", "bf16", gc=16, G=2, N=2, H=28, W=27, stride_h=2, stride_w=2,
+          dilation_h=2, dilation_w=2, softmax=1),
+    small("sp_f16_g8", "f16", gc=8, G=5, N=1, H=17, W=33),
+    small("sp_f32_g4", "f32", gc=4, G=3, N=2, H=9, W=40, softmax=1),
+    small("sp_bf16_g32", "bf16", gc=32, G=2, N=1, H=35, W=18, remove_center=1, softmax=1),
+    small("sp_f32_g64", "f32", gc=64, G=1, N=2, H=13, W=11),
+    small("sp_f16_g128", "f16", gc=128, G=2, N=1, H=9, W=10),
+    small("sp_f32_k5neg", "f32", gc=8, G=2, N=1, H=16, W=16, kernel_h=5, kernel_w=5, pad_h=2,
+          pad_w=2, offset_scale=-0.75),
+    small("sp_f16_1px", "f16", gc=16, G=2, N=3, H=1, W=1),
+    small("sp_f32_s3", "f32", gc=16, G=1, N=1, H=37, W=41, stride_h=3, stride_w=2, pad_h=0),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT, ids=lambda w: w.name)
+@pytest.mark.parametrize("mode", ["window", "halo1", "single_pass"])
+def test_backward_paths(w, mode, monkeypatch):
+    # the windowed kernel, the same with a one-pixel halo (most samples leave
+    # the window and take the far path), and the single-pass atomic kernels
+    if mode in ("window", "halo1"):
+        monkeypatch.setenv("DCN_BWD_WINDOW", "1")
+    if mode == "halo1":
+        monkeypatch.setenv("DCN_BWD_HALO", "1")
+    if mode == "single_pass":
+        monkeypatch.setenv("DCN_BWD_WINDOW", "0")
+    check_bwd(w, make_inputs(w))
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("window", ["1", "0"])
+def test_backward_crowded_samples(dt, window, monkeypatch):
+    # every sample of a 32x32 image aimed at one cell: the cells inside each
+    # tile's window collect hundreds of samples, the rest leave the window
+    monkeypatch.setenv("DCN_BWD_WINDOW", window)
+    w = small(f"crowd_{dt}", dt, gc=16, G=1, N=1, H=32, W=32, softmax=1)
+    t = make_inputs(w)
+    ho = torch.arange(w.H_out).view(-1, 1, 1)
+    wo = torch.arange(w.W_out).view(1, -1, 1)
+    taps = torch.tensor(oracle.taps(oracle_params(w)), dtype=torch.float32)   # (P, 2) as (x, y)
+    # targets jittered inside the cell [16, 17)^2 so that the samples differ
+    # (identical samples would make the DCNv3 mask gradient vanish exactly)
+    jit = torch.rand((w.N, w.H_out, w.W_out, w.G, w.P, 2), generator=torch.Generator().manual_seed(3))
+    off = torch.empty(w.N, w.H_out, w.W_out, w.G, w.P, 2)
+    off[..., 0] = (16.1 - wo - taps[:, 0]).unsqueeze(0).unsqueeze(3) + 0.8 * jit[..., 0]
+    off[..., 1] = (16.1 - ho - taps[:, 1]).unsqueeze(0).unsqueeze(3) + 0.8 * jit[..., 1]
+    t["offset"] = off.to(t["offset"].dtype)
+    check_bwd(w, t)
 
 
 # ---- hand-worked cases and exact identities -----------------------------------
