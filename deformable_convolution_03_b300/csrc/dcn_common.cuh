@@ -36,6 +36,9 @@ struct KParams {
   int softmax;
   long long units;           // N*Ho*Wo*G: one (pixel, group) pair each
   FastDiv div_G, div_Wo, div_Ho;
+  // 2-D tiling of the wide forward: a block covers tile_w x tile_h output
+  // pixels (all groups and channel slices of each); 0 means linear order.
+  int tile_w, tile_h, tiles_w, tiles_h;
   // Kernel taps of the P points, in point order (x-major, centre removed when
   // asked): ix*dilation_w - cen_w and iy*dilation_h - cen_h, as floats (exact).
   float tap_x[DCN_MAX_POINTS];
@@ -115,6 +118,42 @@ template <> struct Dt<__nv_bfloat16> {
   }
   __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
+
+// Loads of data read once (offsets, masks): not kept in L1, so that they do
+// not evict the input lines that neighbouring samples reuse.
+template <typename T> __device__ __forceinline__ float ld_once_1(const T* p);
+template <typename T> __device__ __forceinline__ float2 ld_once_2(const T* p);
+
+template <> __device__ __forceinline__ float ld_once_1<float>(const float* p) {
+  float v;
+  asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+template <> __device__ __forceinline__ float2 ld_once_2<float>(const float* p) {
+  float2 v;
+  asm("ld.global.nc.L1::no_allocate.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+template <> __device__ __forceinline__ float ld_once_1<__half>(const __half* p) {
+  unsigned short h;
+  asm("ld.global.nc.L1::no_allocate.b16 %0, [%1];" : "=h"(h) : "l"(p));
+  return __half2float(__ushort_as_half(h));
+}
+template <> __device__ __forceinline__ float2 ld_once_2<__half>(const __half* p) {
+  uint32_t w;
+  asm("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(w) : "l"(p));
+  return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+template <> __device__ __forceinline__ float ld_once_1<__nv_bfloat16>(const __nv_bfloat16* p) {
+  unsigned short h;
+  asm("ld.global.nc.L1::no_allocate.b16 %0, [%1];" : "=h"(h) : "l"(p));
+  return __uint_as_float((uint32_t)h << 16);
+}
+template <> __device__ __forceinline__ float2 ld_once_2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  uint32_t w;
+  asm("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(w) : "l"(p));
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
 
 // ---- a thread's slice of CPT consecutive channels ---------------------------
 // The slice starts CPT*sizeof(T)-aligned (the host picks CPT so that it is),

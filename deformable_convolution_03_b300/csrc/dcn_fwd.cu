@@ -109,24 +109,46 @@ fwd_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ 
 // The wide kernel: one thread per (unit, slice of CPT channels) where a
 // slice is 16, 32 or 64 bytes and every corner is one or two 256-bit loads.
 // Corners outside the image keep a valid (clamped) address and get weight 0,
-// so every thread runs the same straight-line code for every point.  Needs
-// the unit count and each image's element count below 2^31.
+// so every thread runs the same straight-line code for every point.  With
+// kp.tile_w > 0 a block covers a tile_w x tile_h patch of output pixels (all
+// groups and slices), so that the block's samples share input lines in L1;
+// otherwise it covers 256 consecutive (unit, slice) items.  Offsets and masks
+// are read once and bypass L1.  Needs the unit count and each image's
+// element count below 2^31.
 template <typename T, int CPT, int KP>
 __global__ void __launch_bounds__(256)
 fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ offset,
                 const T* __restrict__ mask, T* __restrict__ output) {
   constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words per corner
   const int chunks = kp.gc / CPT;
-  const uint32_t item = blockIdx.x * blockDim.x + threadIdx.x;
-  if (item >= (uint32_t)(kp.units * chunks)) return;
-  const uint32_t unit = chunks == 1 ? item : item / (uint32_t)chunks;
-  const int c0 = (int)(item - unit * chunks) * CPT;
-  const uint32_t q1 = kp.div_G.div(unit);
-  const int g = (int)(unit - q1 * (uint32_t)kp.G);
-  const uint32_t q2 = kp.div_Wo.div(q1);
-  const int wo = (int)(q1 - q2 * (uint32_t)kp.Wo);
-  const uint32_t n = kp.div_Ho.div(q2);
-  const int ho = (int)(q2 - n * (uint32_t)kp.Ho);
+  uint32_t unit, n;
+  int c0, g, ho, wo;
+  if (kp.tile_w > 0) {
+    // tid = (pixel-in-tile * G + g) * chunks + slice
+    const int per_px = kp.G * chunks;
+    const int lp = threadIdx.x / per_px, r = threadIdx.x - lp * per_px;
+    g = r / chunks;
+    c0 = (r - g * chunks) * CPT;
+    const int tiles = kp.tiles_w * kp.tiles_h;
+    n = blockIdx.x / tiles;
+    const int t = blockIdx.x - n * tiles;
+    const int ty = t / kp.tiles_w;
+    ho = ty * kp.tile_h + lp / kp.tile_w;
+    wo = (t - ty * kp.tiles_w) * kp.tile_w + lp % kp.tile_w;
+    if (ho >= kp.Ho || wo >= kp.Wo) return;
+    unit = ((n * (uint32_t)kp.Ho + ho) * kp.Wo + wo) * kp.G + g;
+  } else {
+    const uint32_t item = blockIdx.x * blockDim.x + threadIdx.x;
+    if (item >= (uint32_t)(kp.units * chunks)) return;
+    unit = chunks == 1 ? item : item / (uint32_t)chunks;
+    c0 = (int)(item - unit * chunks) * CPT;
+    const uint32_t q1 = kp.div_G.div(unit);
+    g = (int)(unit - q1 * (uint32_t)kp.G);
+    const uint32_t q2 = kp.div_Wo.div(q1);
+    wo = (int)(q1 - q2 * (uint32_t)kp.Wo);
+    n = kp.div_Ho.div(q2);
+    ho = (int)(q2 - n * (uint32_t)kp.Ho);
+  }
 
   const int P = KP > 0 ? KP : kp.P;
   const T* mrow = mask + (size_t)unit * P;
@@ -153,9 +175,9 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
 
 #pragma unroll(KP > 0 ? KP : 3)
   for (int p = 0; p < P; ++p) {
-    float m = Dt<T>::one(mrow + p);
+    float m = ld_once_1(mrow + p);
     if (kp.softmax) m = expf(m - mx) * inv;
-    const float2 d = Dt<T>::two(orow + 2 * p);
+    const float2 d = ld_once_2(orow + 2 * p);
     float x = location(d.x, kp.tap_x[p], scale, ref_x);
     float y = location(d.y, kp.tap_y[p], scale, ref_y);
     if (!in_box(x, y, kp.W, kp.H)) {  // also NaN / inf: every corner falls outside
@@ -203,7 +225,9 @@ static cudaError_t launch_fwd_t(const KParams& kp, int cpt, const void* in, cons
                                 const void* msk, void* out, cudaStream_t s) {
   const long long items = kp.units * (kp.gc / (cpt < 0 ? -cpt : cpt));
   const int block = 256;
-  const long long grid = (items + block - 1) / block;
+  const long long grid = (cpt < 0 && kp.tile_w > 0)
+                             ? (long long)kp.N * kp.tiles_w * kp.tiles_h
+                             : (items + block - 1) / block;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   const T* i_ = static_cast<const T*>(in);
   const T* o_ = static_cast<const T*>(off);

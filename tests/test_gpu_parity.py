@@ -106,8 +106,11 @@ def test_every_general_kernel_instance(dt, cap, monkeypatch):
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("gc", [4, 8, 16, 24, 48])
 @pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
-def test_wide_forward_instances(dt, gc, sm, rc):
-    # slices of 4, 8 and 16 channels, 9 points and the runtime point count
+@pytest.mark.parametrize("tile", ["1", "0"])
+def test_wide_forward_instances(dt, gc, sm, rc, tile, monkeypatch):
+    # slices of 4, 8 and 16 channels, 9 points and the runtime point count,
+    # blocks over 2-D pixel tiles and over consecutive items
+    monkeypatch.setenv("DCN_FWD_TILE", tile)
     w = small(f"wide_{dt}_{gc}", dt, gc=gc, G=3, softmax=sm, remove_center=rc, N=2, H=11, W=13)
     check_fwd(w, make_inputs(w))
 
