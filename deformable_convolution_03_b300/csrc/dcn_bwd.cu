@@ -19,6 +19,7 @@
 // caller's float32 grad_input, or into a float32 workspace that a second
 // kernel rounds to the storage dtype.
 #include <climits>
+#include <cstdlib>
 
 #include "dcn_common.cuh"
 #include "dcn_kernels.h"
@@ -73,11 +74,30 @@ __device__ __forceinline__ void red_add(float* dst, const float (&v)[CPT]) {
 
 // One thread per (unit, slice of CPT channels); gc/CPT is a power of two no
 // larger than 32, so the threads of a unit are adjacent lanes of one warp.
+// Copy n elements of T from shared to global memory with 16-byte stores when
+// both ends allow it (the caller's block then writes whole sectors).
+template <typename T>
+__device__ __forceinline__ void block_copy_out(T* __restrict__ dst, const T* __restrict__ src,
+                                               int n) {
+  const int bytes = n * (int)sizeof(T);
+  if ((reinterpret_cast<uintptr_t>(dst) & 15) == 0 && (bytes & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = threadIdx.x; i < bytes / 16; i += blockDim.x) d4[i] = s4[i];
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+  }
+}
+
 template <typename T, int CPT>
 __global__ void __launch_bounds__(256)
 bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ input,
            const T* __restrict__ offset, const T* __restrict__ mask, float* __restrict__ gin,
-           T* __restrict__ goff, T* __restrict__ gmask) {
+           T* __restrict__ goff, T* __restrict__ gmask, int stage) {
+  // stage != 0: grad_offset / grad_mask rows of the block's units are put
+  // together in shared memory and written out at the end with full-sector
+  // stores instead of one 2- or 4-byte store per value
+  extern __shared__ __align__(16) unsigned char stage_raw[];
   const int chunks = kp.gc / CPT;
   const long long item = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const bool active = item < kp.units * chunks;
@@ -107,6 +127,11 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
 
   float gm_row[DCN_MAX_POINTS];
   float dot = 0.f;
+  T* s_off = reinterpret_cast<T*>(stage_raw);
+  T* s_mask = s_off + (blockDim.x / chunks) * kp.P * 2;
+  const int lunit = threadIdx.x / chunks;
+  T* so_row = s_off + lunit * kp.P * 2;
+  T* sm_row = s_mask + lunit * kp.P;
 
 #pragma unroll 1
   for (int p = 0; p < kp.P; ++p) {
@@ -160,21 +185,31 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
         gox = scale * m * (gy * (dk[1] - dk[0]) + fy * (dk[3] - dk[2]));
         goy = scale * m * (gx * (dk[2] - dk[0]) + fx * (dk[3] - dk[1]));
       }
-      T* go2 = goff + (unit * kp.P + p) * 2;
+      T* go2 = stage ? so_row + p * 2 : goff + (unit * kp.P + p) * 2;
       go2[0] = Dt<T>::from_f(gox);
       go2[1] = Dt<T>::from_f(goy);
       if (kp.softmax) {
         gm_row[p] = gm;
         dot = fmaf(m, gm, dot);
       } else {
-        gmask[unit * kp.P + p] = Dt<T>::from_f(gm);
+        (stage ? sm_row : gmask + unit * kp.P)[p] = Dt<T>::from_f(gm);
       }
     }
   }
   if (leader && kp.softmax) {
     for (int p = 0; p < kp.P; ++p) {
       const float m = expf(Dt<T>::one(mrow + p) - mx) * inv;
-      gmask[unit * kp.P + p] = Dt<T>::from_f(m * (gm_row[p] - dot));
+      (stage ? sm_row : gmask + unit * kp.P)[p] = Dt<T>::from_f(m * (gm_row[p] - dot));
+    }
+  }
+  if (stage) {
+    __syncthreads();
+    const int per_block = blockDim.x / chunks;
+    const long long u0 = (long long)blockIdx.x * per_block;
+    const int nu = (int)min((long long)per_block, kp.units - u0);
+    if (nu > 0) {
+      block_copy_out(goff + u0 * kp.P * 2, s_off, nu * kp.P * 2);
+      block_copy_out(gmask + u0 * kp.P, s_mask, nu * kp.P);
     }
   }
 }
@@ -274,6 +309,12 @@ round_kernel(const float* __restrict__ acc, T* __restrict__ out, long long n) {
   for (; i < n; i += stride) out[i] = Dt<T>::from_f(acc[i]);
 }
 
+// DCN_BWD_STAGE=0 writes grad_offset / grad_mask directly (for comparison).
+static int env_stage() {
+  const char* v = std::getenv("DCN_BWD_STAGE");
+  return !(v && v[0] == '0');
+}
+
 template <typename T>
 static cudaError_t launch_bwd_t(const KParams& kp, int cpt, const void* gout, const void* in,
                                 const void* off, const void* msk, float* gin_acc, void* gin,
@@ -289,11 +330,14 @@ static cudaError_t launch_bwd_t(const KParams& kp, int cpt, const void* gout, co
   const long long grid = (items + block - 1) / block;
   if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
   switch (cpt) {
-#define DCN_CASE(K)                                                                          \
-    case K:                                                                                  \
-      bwd_kernel<T, K><<<(unsigned)grid, block, 0, s>>>(kp, go_, i_, o_, m_, gin_acc, goff_, \
-                                                        gm_);                                \
-      break;
+#define DCN_CASE(K)                                                                        \
+    case K: {                                                                              \
+      const size_t st = (size_t)(block / (kp.gc / K)) * kp.P * 3 * sizeof(T);             \
+      const int stage = st <= 48 * 1024 && env_stage();                                    \
+      bwd_kernel<T, K><<<(unsigned)grid, block, stage ? st : 0, s>>>(                      \
+          kp, go_, i_, o_, m_, gin_acc, goff_, gm_, stage);                                \
+      break;                                                                               \
+    }
     DCN_CASE(1) DCN_CASE(2) DCN_CASE(4) DCN_CASE(8) DCN_CASE(16) DCN_CASE(32)
 #undef DCN_CASE
     case 0:
