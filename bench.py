@@ -39,6 +39,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from deformable_convolution_03_b300 import binding as B  # noqa: E402
+from deformable_convolution_03_b300.replicas import (  # noqa: E402
+    aggregate_gbs, max_over_ranks, rank_seed)
 from deformable_convolution_03_b300.inputs import (  # noqa: E402
     DTYPES, T_DEPTHS, WORKLOADS, Workload, ideal_bytes, make_inputs)
 
@@ -51,9 +53,9 @@ FALLBACK_HBM_GBS = 6400.0
 # source voids the figure.
 TRAFFIC = {
     # profiles/fwd_wide_t_stage1_f16.md
-    "fwd@t_stage1_f16": {"bytes": 69_075_200 + 6_083_328, "sha": "44766e2214a2"},
+    "fwd@t_stage1_f16": {"bytes": 69_104_384 + 3_520_256, "sha": "819c2d87b4e4"},
     # profiles/bwd_kernel_t_stage1_f16.md: bwd_kernel + round_kernel (the memset is not a kernel)
-    "bwd@t_stage1_f16": {"bytes": 146_137_088 + 48_210_432 + 51_387_136 + 1_556_736, "sha": "09a7ce77d4d5"},
+    "bwd@t_stage1_f16": {"bytes": 146_143_232 + 51_331_840 + 51_386_368 + 1_508_864, "sha": "ceb5ed66dbc1"},
 }
 
 
@@ -174,9 +176,9 @@ class ClockSampler:
 class Case:
     """Device tensors, outputs and workspace of one workload."""
 
-    def __init__(self, w: Workload, dev):
+    def __init__(self, w: Workload, dev, rank: int = 0):
         self.w, self.dev = w, dev
-        t = make_inputs(w, grad=True)
+        t = make_inputs(w, seed=rank_seed(w.seed, rank), grad=True)
         self.host = t
         self.p = B.Params(dtype=B.TORCH_TO_DCN[DTYPES[w.dtype]], **w.params())
         self.x = {k: v.to(dev) for k, v in t.items()}
@@ -383,7 +385,7 @@ def main():
     torch.cuda.set_device(dev)
 
     w = WORKLOADS[args.workload]
-    case = Case(w, dev)
+    case = Case(w, dev, rank)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
@@ -407,26 +409,18 @@ def main():
 
     fwd_ms = statistics.mean(t["fwd"])
     bwd_ms = statistics.mean(t["bwd"])
-    step_ms = fwd_ms + bwd_ms
-    if dist is not None:
-        v = torch.tensor([step_ms, fwd_ms, bwd_ms], device=dev)
-        dist.all_reduce(v, op=dist.ReduceOp.MAX)
-        step_ms, fwd_ms, bwd_ms = v.tolist()
+    step_ms, fwd_ms, bwd_ms = max_over_ranks([fwd_ms + bwd_ms, fwd_ms, bwd_ms], dist, dev)
 
     ib = ideal_bytes(w)
     step_bytes = ib["fwd"] + ib["bwd"]
-    value = world * step_bytes / (step_ms * 1e-3) / 1e9
+    value = aggregate_gbs(step_bytes, world, step_ms)
 
     # end to end through host buffers
     e2e = None
     if args.e2e_steps > 0:
         e2e_t, h2d, d2h = e2e_steps(case, args.e2e_steps, flush)
-        e2e_ms = statistics.median(e2e_t)
-        if dist is not None:
-            v = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(v, op=dist.ReduceOp.MAX)
-            e2e_ms = v.item()
-        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+        e2e_ms = max_over_ranks([statistics.median(e2e_t)], dist, dev)[0]
+        e2e = {"value": round(aggregate_gbs(step_bytes, world, e2e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e2e_ms, 4)}
 
