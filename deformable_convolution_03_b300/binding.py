@@ -30,8 +30,9 @@ DCN_MAX_POINTS = 64
 TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: DCN_BF16}
 
 # Every symbol include/dcn_core.h declares.
-EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_bwd_workspace",
-           "dcn_core_bwd", "dcn_core_bwd_noalloc", "dcn_status_str", "dcn_version")
+EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
+           "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
+           "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -93,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.dcn_core_bwd_workspace.restype = ctypes.c_size_t
         L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
+        L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t,
+                                      vp]
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -162,6 +166,27 @@ def dcn_core_bwd(p: Params, grad_out, input, offset, mask, grad_input, grad_offs
                               _ptr(mask), _ptr(grad_input), _ptr(grad_offset), _ptr(grad_mask),
                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
            "dcn_core_bwd")
+
+
+def dcn_core_fwd_om(p: Params, input, offset_mask, row_stride: int, output, stream=None) -> None:
+    """Forward with DCNv4's merged offset/mask tensor (N, Ho, Wo, G, row_stride)."""
+    _check(lib().dcn_core_fwd_om(ctypes.byref(p.c()), _ptr(input), _ptr(offset_mask),
+                                 int(row_stride), _ptr(output), _stream(stream)),
+           "dcn_core_fwd_om")
+
+
+def dcn_core_bwd_om(p: Params, grad_out, input, offset_mask, row_stride: int, grad_input,
+                    grad_offset_mask, workspace=None, workspace_bytes: int | None = None,
+                    stream=None) -> None:
+    """Backward with the merged layout; grad_offset_mask has offset_mask's layout."""
+    if workspace_bytes is None:
+        workspace_bytes = (workspace.numel() * workspace.element_size()
+                           if isinstance(workspace, torch.Tensor) else 0)
+    _check(lib().dcn_core_bwd_om(ctypes.byref(p.c()), _ptr(grad_out), _ptr(input),
+                                 _ptr(offset_mask), int(row_stride), _ptr(grad_input),
+                                 _ptr(grad_offset_mask), _ptr(workspace), int(workspace_bytes),
+                                 _stream(stream)),
+           "dcn_core_bwd_om")
 
 
 def dcn_core_bwd_noalloc(p: Params, grad_out, input, offset, mask, grad_input, grad_offset,

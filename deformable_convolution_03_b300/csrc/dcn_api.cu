@@ -93,6 +93,9 @@ void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
   kp->offset_scale = p->offset_scale;
   kp->softmax = p->softmax;
   kp->units = g.units;
+  kp->os_off = 2 * g.P;
+  kp->os_mask = g.P;
+  kp->merged = 0;
   kp->div_G = fast_div((uint32_t)p->G);
   kp->div_Wo = fast_div((uint32_t)g.Wo);
   kp->div_Ho = fast_div((uint32_t)g.Ho);
@@ -290,11 +293,19 @@ int dcn_num_points(const dcn_params_t* p) {
   return rc != DCN_OK ? -rc : g.P;
 }
 
-int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
-                 void* output, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Both layouts of the offsets and masks: separate tensors (row strides 2P and
+// P) or one merged tensor (offset row, then mask row, in rows of
+// row_stride elements).
+int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
+             void* output, void* stream, int row_stride) {
   Geometry g;
   int rc = validate(p, &g);
   if (rc != DCN_OK) return rc;
+  if (row_stride && (row_stride < 3 * g.P || row_stride % 2)) return DCN_ERR_SHAPE;
   if (g.units == 0) return DCN_OK;
   if (!input || !offset || !mask || !output) return DCN_ERR_NULL;
   const size_t es = (size_t)elem_size(p->dtype);
@@ -303,11 +314,34 @@ int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, c
     return DCN_ERR_ALIGN;
   dcn::KParams kp;
   fill_kparams(p, g, &kp);
+  if (row_stride) {
+    kp.os_off = kp.os_mask = row_stride;
+    kp.merged = 1;
+  }
   const int cpt = pick_fwd_cpt(p, g, input, output);
   if (cpt < 0) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
   return cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
+                 void* output, void* stream) {
+  return core_fwd(p, input, offset, mask, output, stream, 0);
+}
+
+int dcn_core_fwd_om(const dcn_params_t* p, const void* input, const void* offset_mask,
+                    int row_stride, void* output, void* stream) {
+  if (row_stride <= 0) return p ? DCN_ERR_SHAPE : DCN_ERR_NULL;
+  const int P = dcn_num_points(p);
+  if (P < 0) return -P;
+  const size_t es = (size_t)elem_size(p->dtype);
+  const char* om = static_cast<const char*>(offset_mask);
+  return core_fwd(p, input, om, om ? om + 2 * P * es : nullptr, output, stream, row_stride);
 }
 
 size_t dcn_core_bwd_workspace(const dcn_params_t* p) {
@@ -316,12 +350,17 @@ size_t dcn_core_bwd_workspace(const dcn_params_t* p) {
   return p->dtype == DCN_F32 ? 0 : (size_t)g.n_in * sizeof(float);
 }
 
-int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
-                 const void* offset, const void* mask, void* grad_input, void* grad_offset,
-                 void* grad_mask, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, const void* offset,
+             const void* mask, void* grad_input, void* grad_offset, void* grad_mask,
+             void* workspace, size_t workspace_bytes, void* stream, int row_stride) {
   Geometry g;
   int rc = validate(p, &g);
   if (rc != DCN_OK) return rc;
+  if (row_stride && (row_stride < 3 * g.P || row_stride % 2)) return DCN_ERR_SHAPE;
   if (g.units == 0) return DCN_OK;
   if (!grad_out || !input || !offset || !mask || !grad_input || !grad_offset || !grad_mask)
     return DCN_ERR_NULL;
@@ -341,6 +380,10 @@ int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
   }
   dcn::KParams kp;
   fill_kparams(p, g, &kp);
+  if (row_stride) {
+    kp.os_off = kp.os_mask = row_stride;
+    kp.merged = 1;
+  }
   dcn::WinGeom wg;
   const int wcpt = plan_window(p, g, input, grad_out, acc, &wg);
   const int cpt = wcpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
@@ -355,6 +398,32 @@ int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
                                               mask, acc, grad_input, grad_offset, grad_mask, s));
   return cuda_status(dcn::launch_bwd(kp, p->dtype, cpt, grad_out, input, offset, mask, acc,
                                      grad_input, grad_offset, grad_mask, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
+                 const void* offset, const void* mask, void* grad_input, void* grad_offset,
+                 void* grad_mask, void* workspace, size_t workspace_bytes, void* stream) {
+  return core_bwd(p, grad_out, input, offset, mask, grad_input, grad_offset, grad_mask,
+                  workspace, workspace_bytes, stream, 0);
+}
+
+int dcn_core_bwd_om(const dcn_params_t* p, const void* grad_out, const void* input,
+                    const void* offset_mask, int row_stride, void* grad_input,
+                    void* grad_offset_mask, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (row_stride <= 0) return p ? DCN_ERR_SHAPE : DCN_ERR_NULL;
+  const int P = dcn_num_points(p);
+  if (P < 0) return -P;
+  const size_t es = (size_t)elem_size(p->dtype);
+  const char* om = static_cast<const char*>(offset_mask);
+  char* gom = static_cast<char*>(grad_offset_mask);
+  return core_bwd(p, grad_out, input, om, om ? om + 2 * P * es : nullptr, grad_input, gom,
+                  gom ? gom + 2 * P * es : nullptr, workspace, workspace_bytes, stream,
+                  row_stride);
 }
 
 const char* dcn_status_str(int status) {

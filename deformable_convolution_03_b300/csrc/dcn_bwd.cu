@@ -114,8 +114,8 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
 #pragma unroll
     for (int i = 0; i < CPT; ++i) go[i] = 0.f;
   }
-  const T* mrow = mask + unit * kp.P;
-  const T* orow = offset + unit * kp.P * 2;
+  const T* mrow = mask + unit * kp.os_mask;
+  const T* orow = offset + unit * kp.os_off;
   float mx = 0.f, inv = 1.f;
   if (kp.softmax && active) softmax_stats_b(mrow, kp.P, mx, inv);
 
@@ -185,23 +185,25 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
         gox = scale * m * (gy * (dk[1] - dk[0]) + fy * (dk[3] - dk[2]));
         goy = scale * m * (gx * (dk[2] - dk[0]) + fx * (dk[3] - dk[1]));
       }
-      T* go2 = stage ? so_row + p * 2 : goff + (unit * kp.P + p) * 2;
+      T* go2 = stage ? so_row + p * 2 : goff + unit * kp.os_off + p * 2;
       go2[0] = Dt<T>::from_f(gox);
       go2[1] = Dt<T>::from_f(goy);
       if (kp.softmax) {
         gm_row[p] = gm;
         dot = fmaf(m, gm, dot);
       } else {
-        (stage ? sm_row : gmask + unit * kp.P)[p] = Dt<T>::from_f(gm);
+        (stage ? sm_row : gmask + unit * kp.os_mask)[p] = Dt<T>::from_f(gm);
       }
     }
   }
   if (leader && kp.softmax) {
     for (int p = 0; p < kp.P; ++p) {
       const float m = expf(Dt<T>::one(mrow + p) - mx) * inv;
-      (stage ? sm_row : gmask + unit * kp.P)[p] = Dt<T>::from_f(m * (gm_row[p] - dot));
+      (stage ? sm_row : gmask + unit * kp.os_mask)[p] = Dt<T>::from_f(m * (gm_row[p] - dot));
     }
   }
+  if (leader && kp.merged)
+    for (int i = 3 * kp.P; i < kp.os_off; ++i) goff[unit * kp.os_off + i] = Dt<T>::from_f(0.f);
   if (stage) {
     __syncthreads();
     const int per_block = blockDim.x / chunks;
@@ -223,8 +225,8 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
   const long long unit = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (unit >= kp.units) return;
   const UnitB u = decompose_b(unit, kp);
-  const T* mrow = mask + unit * kp.P;
-  const T* orow = offset + unit * kp.P * 2;
+  const T* mrow = mask + unit * kp.os_mask;
+  const T* orow = offset + unit * kp.os_off;
   const T* grow = gout + unit * kp.gc;
   float mx = 0.f, inv = 1.f;
   if (kp.softmax) softmax_stats_b(mrow, kp.P, mx, inv);
@@ -262,14 +264,16 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
       gox = scale * m * (gy * (dk[1] - dk[0]) + fy * (dk[3] - dk[2]));
       goy = scale * m * (gx * (dk[2] - dk[0]) + fx * (dk[3] - dk[1]));
     }
-    T* go2 = goff + (unit * kp.P + p) * 2;
+    T* go2 = goff + unit * kp.os_off + p * 2;
     go2[0] = Dt<T>::from_f(gox);
     go2[1] = Dt<T>::from_f(goy);
     // without softmax dL/dm is the result; with softmax it is needed again
     // after the loop, and the second pass below recomputes it.
-    if (!kp.softmax) gmask[unit * kp.P + p] = Dt<T>::from_f(gm);
+    if (!kp.softmax) gmask[unit * kp.os_mask + p] = Dt<T>::from_f(gm);
     dot = fmaf(m, gm, dot);
   }
+  if (kp.merged)
+    for (int i = 3 * kp.P; i < kp.os_off; ++i) goff[unit * kp.os_off + i] = Dt<T>::from_f(0.f);
   if (!kp.softmax) return;
   // Second pass for the softmax derivative: dL/dm_p is recomputed, since a
   // per-point array would not fit in registers for large P.
@@ -296,7 +300,7 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
         gm = fmaf(w[k], s, gm);
       }
     }
-    gmask[unit * kp.P + p] = Dt<T>::from_f(m * (gm - dot));
+    gmask[unit * kp.os_mask + p] = Dt<T>::from_f(m * (gm - dot));
   }
 }
 
@@ -333,7 +337,7 @@ static cudaError_t launch_bwd_t(const KParams& kp, int cpt, const void* gout, co
 #define DCN_CASE(K)                                                                        \
     case K: {                                                                              \
       const size_t st = (size_t)(block / (kp.gc / K)) * kp.P * 3 * sizeof(T);             \
-      const int stage = st <= 48 * 1024 && env_stage();                                    \
+      const int stage = st <= 48 * 1024 && !kp.merged && env_stage();                                    \
       bwd_kernel<T, K><<<(unsigned)grid, block, stage ? st : 0, s>>>(                      \
           kp, go_, i_, o_, m_, gin_acc, goff_, gm_, stage);                                \
       break;                                                                               \

@@ -82,8 +82,8 @@ bwd_window_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout
   const int c0 = slice * CPT;
   const long long unit =
       active ? (((long long)n * kp.Ho + ho) * kp.Wo + wo) * kp.G + g : 0;
-  const T* mrow = mask + unit * P;
-  const T* orow = offset + unit * P * 2;
+  const T* mrow = mask + unit * kp.os_mask;
+  const T* orow = offset + unit * kp.os_off;
   const size_t img_off = (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
   const T* img = input + img_off;
   const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
@@ -166,23 +166,25 @@ bwd_window_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout
         gox = scale * m * (gy * (dk[1] - dk[0]) + fy * (dk[3] - dk[2]));
         goy = scale * m * (gx * (dk[2] - dk[0]) + fx * (dk[3] - dk[1]));
       }
-      T* go2 = goff + (unit * P + p) * 2;
+      T* go2 = goff + unit * kp.os_off + p * 2;
       go2[0] = Dt<T>::from_f(gox);
       go2[1] = Dt<T>::from_f(goy);
       if (kp.softmax) {
         gm_row[p] = gm;
         dot = fmaf(m, gm, dot);
       } else {
-        gmask[unit * P + p] = Dt<T>::from_f(gm);
+        gmask[unit * kp.os_mask + p] = Dt<T>::from_f(gm);
       }
     }
   }
   if (leader && kp.softmax) {
     for (int p = 0; p < P; ++p) {
       const float m = expf(Dt<T>::one(mrow + p) - mx) * inv;
-      gmask[unit * P + p] = Dt<T>::from_f(m * (gm_row[p] - dot));
+      gmask[unit * kp.os_mask + p] = Dt<T>::from_f(m * (gm_row[p] - dot));
     }
   }
+  if (leader && kp.merged)
+    for (int i = 3 * P; i < kp.os_off; ++i) goff[unit * kp.os_off + i] = Dt<T>::from_f(0.f);
   // per-cell counts, and the far samples' share of grad_input straight to memory
   if (active) {
     for (int p = 0; p < P; ++p) {

@@ -39,6 +39,11 @@ struct KParams {
   // 2-D tiling of the wide forward: a block covers tile_w x tile_h output
   // pixels (all groups and channel slices of each); 0 means linear order.
   int tile_w, tile_h, tiles_w, tiles_h;
+  // Elements between consecutive units' offset rows and mask rows: 2P and P
+  // for separate tensors; the row stride of the merged offset/mask tensor
+  // (mask = offset + 2P) when merged != 0, whose gradient rows then also get
+  // their padding (elements 3P .. stride-1) written as zero.
+  int os_off, os_mask, merged;
   // Kernel taps of the P points, in point order (x-major, centre removed when
   // asked): ix*dilation_w - cen_w and iy*dilation_h - cen_h, as floats (exact).
   float tap_x[DCN_MAX_POINTS];

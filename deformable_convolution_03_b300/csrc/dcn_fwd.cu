@@ -64,8 +64,8 @@ fwd_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ 
   const int c0 = (int)(item - unit * chunks) * CPT;
   const Unit u = decompose(unit, kp);
 
-  const T* mrow = mask + unit * kp.P;
-  const T* orow = offset + unit * kp.P * 2;
+  const T* mrow = mask + unit * kp.os_mask;
+  const T* orow = offset + unit * kp.os_off;
   float mx = 0.f, inv = 1.f;
   if (kp.softmax) softmax_stats(mrow, kp.P, mx, inv);
 
@@ -151,8 +151,8 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
   }
 
   const int P = KP > 0 ? KP : kp.P;
-  const T* mrow = mask + (size_t)unit * P;
-  const T* orow = offset + (size_t)unit * P * 2;
+  const T* mrow = mask + (size_t)unit * kp.os_mask;
+  const T* orow = offset + (size_t)unit * kp.os_off;
   const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
   const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
   const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);

@@ -123,6 +123,28 @@ int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
                  const void* offset, const void* mask, void* grad_input, void* grad_offset,
                  void* grad_mask, void* workspace, size_t workspace_bytes, void* stream);
 
+/* DCNv4's merged offset / mask layout: the projection that predicts the
+ * offsets and the weights is one linear layer, so they arrive as one tensor
+ * (page "告别DCNv3的卡顿：实测DCNv4在A100上3倍提速，手把手教你集成到FlashInternImage",
+ * section 1: the offset and weight computations are merged).
+ *   offset_mask (N, H_out, W_out, G, row_stride): for each (pixel, group) a
+ *   row of 2P offsets ((dx, dy) per point, as in dcn_core_fwd) followed by P
+ *   mask values, then row_stride - 3P padding elements (ignored).
+ * row_stride >= 3P and even (e.g. 32 for P = 9, a 64-byte row in 16-bit).
+ * offset_mask aligned to 2 elements.  Same computation, results and errors as
+ * dcn_core_fwd; DCN_ERR_SHAPE for a bad row_stride. */
+int dcn_core_fwd_om(const dcn_params_t* p, const void* input, const void* offset_mask,
+                    int row_stride, void* output, void* stream);
+
+/* The backward in the merged layout: grad_offset_mask has offset_mask's
+ * layout, gradients of the offsets then of the mask (or logits) in each row,
+ * and its padding elements are written as zero (the tensor is fully
+ * overwritten).  Otherwise as dcn_core_bwd. */
+int dcn_core_bwd_om(const dcn_params_t* p, const void* grad_out, const void* input,
+                    const void* offset_mask, int row_stride, void* grad_input,
+                    void* grad_offset_mask, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
 /* Size of the library's own device scratch array used by
  * dcn_core_bwd_noalloc: 32 MiB, enough for the float32 grad_input accumulator
  * of 8M input elements (N*H*W*G*gc <= 8388608). */

@@ -165,3 +165,19 @@ def test_status_strings(native):
     for code in range(9):
         assert native.dcn_status_str(code).startswith("DCN_")
     assert "unknown" in native.dcn_status_str(99)
+
+
+def test_merged_layout_argument_checks(native):
+    lib = native.lib()
+    p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)   # P = 9
+    for stride in (26, 27, 0, -4):   # below 3P, odd, non-positive
+        assert lib.dcn_core_fwd_om(ctypes.byref(p.c()), A, A, stride, A, None) == native.DCN_ERR_SHAPE
+        assert lib.dcn_core_bwd_om(ctypes.byref(p.c()), A, A, A, stride, A, A, A, 1 << 30,
+                                   None) == native.DCN_ERR_SHAPE
+    assert lib.dcn_core_fwd_om(ctypes.byref(p.c()), A, None, 32, A, None) == native.DCN_ERR_NULL
+    assert lib.dcn_core_fwd_om(None, A, A, 32, A, None) == native.DCN_ERR_NULL
+    assert lib.dcn_core_fwd_om(ctypes.byref(p.c()), A, A + 2, 32, A, None) == native.DCN_ERR_ALIGN
+    assert lib.dcn_core_bwd_om(ctypes.byref(p.c()), A, A, A, 32, A, None, A, 1 << 30,
+                               None) == native.DCN_ERR_NULL
+    bad = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=7)
+    assert lib.dcn_core_fwd_om(ctypes.byref(bad.c()), A, A, 32, A, None) == native.DCN_ERR_DTYPE
