@@ -173,30 +173,66 @@ class ClockSampler:
 
 # ---- one workload on the device ----------------------------------------------
 
-class Case:
-    """Device tensors, outputs and workspace of one workload."""
+def merged_stride(P: int) -> int:
+    """Row stride of the merged offset/mask tensor: 3P rounded up to 16 elements."""
+    return (3 * P + 15) // 16 * 16
 
-    def __init__(self, w: Workload, dev, rank: int = 0):
-        self.w, self.dev = w, dev
+
+class Case:
+    """Device tensors, outputs and workspace of one workload.  layout "merged"
+    feeds offsets and masks as DCNv4's single offset/mask tensor."""
+
+    def __init__(self, w: Workload, dev, rank: int = 0, layout: str = "separate"):
+        self.w, self.dev, self.layout = w, dev, layout
         t = make_inputs(w, seed=rank_seed(w.seed, rank), grad=True)
+        if layout == "merged":
+            rs = self.stride = merged_stride(w.P)
+            o, m = t.pop("offset"), t.pop("mask")
+            pad = torch.zeros(o.shape[:4] + (rs - 3 * w.P,), dtype=o.dtype)
+            t["offset_mask"] = torch.cat([o.flatten(-2), m, pad], -1).contiguous()
         self.host = t
         self.p = B.Params(dtype=B.TORCH_TO_DCN[DTYPES[w.dtype]], **w.params())
         self.x = {k: v.to(dev) for k, v in t.items()}
         self.out = torch.empty(w.N, w.H_out, w.W_out, w.C, dtype=DTYPES[w.dtype], device=dev)
         self.gi = torch.empty_like(self.x["input"])
-        self.go = torch.empty_like(self.x["offset"])
-        self.gm = torch.empty_like(self.x["mask"])
+        if layout == "merged":
+            self.go = torch.empty_like(self.x["offset_mask"])
+            self.gm = None
+        else:
+            self.go = torch.empty_like(self.x["offset"])
+            self.gm = torch.empty_like(self.x["mask"])
         self.ws_bytes = B.dcn_core_bwd_workspace(self.p)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def fwd(self, x=None):
         x = x or self.x
-        B.dcn_core_fwd(self.p, x["input"], x["offset"], x["mask"], self.out)
+        if self.layout == "merged":
+            B.dcn_core_fwd_om(self.p, x["input"], x["offset_mask"], self.stride, self.out)
+        else:
+            B.dcn_core_fwd(self.p, x["input"], x["offset"], x["mask"], self.out)
 
     def bwd(self, x=None):
         x = x or self.x
-        B.dcn_core_bwd(self.p, x["grad_out"], x["input"], x["offset"], x["mask"], self.gi,
-                       self.go, self.gm, self.ws, self.ws_bytes)
+        if self.layout == "merged":
+            B.dcn_core_bwd_om(self.p, x["grad_out"], x["input"], x["offset_mask"], self.stride,
+                              self.gi, self.go, self.ws, self.ws_bytes)
+        else:
+            B.dcn_core_bwd(self.p, x["grad_out"], x["input"], x["offset"], x["mask"], self.gi,
+                           self.go, self.gm, self.ws, self.ws_bytes)
+
+    def results(self):
+        return [t for t in (self.out, self.gi, self.go, self.gm) if t is not None]
+
+    def ideal(self) -> dict:
+        """Ideal bytes; the merged tensor is counted with its padding."""
+        ib = ideal_bytes(self.w)
+        if self.layout == "merged":
+            es = torch.empty((), dtype=DTYPES[self.w.dtype]).element_size()
+            rows = self.w.N * self.w.H_out * self.w.W_out * self.w.G
+            sep = rows * 3 * self.w.P * es
+            mer = rows * self.stride * es
+            ib = {"fwd": ib["fwd"] - sep + mer, "bwd": ib["bwd"] - 2 * sep + 2 * mer}
+        return ib
 
     def launches_per_step(self) -> int:
         # forward kernel; backward kernel; the rounding kernel of 16-bit grad_input
@@ -221,8 +257,7 @@ def timed_steps(case: Case, steps: int, flush: torch.Tensor, phases=("fwd", "bwd
 def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
     """The step through host buffers: pinned inputs in, every result out."""
     hin = {k: v.pin_memory() for k, v in case.host.items()}
-    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-            for t in (case.out, case.gi, case.go, case.gm)]
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in case.results()]
     dev = {k: torch.empty_like(v) for k, v in case.x.items()}
     h2d = sum(v.numel() * v.element_size() for v in hin.values())
     d2h = sum(v.numel() * v.element_size() for v in hout)
@@ -235,7 +270,7 @@ def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
             dev[key].copy_(hin[key], non_blocking=True)
         case.fwd(dev)
         case.bwd(dev)
-        for h, d in zip(hout, (case.out, case.gi, case.go, case.gm)):
+        for h, d in zip(hout, case.results()):
             h.copy_(d, non_blocking=True)
         b.record()
         b.synchronize()
@@ -361,6 +396,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="t_stage1_f16")
+    ap.add_argument("--layout", default="separate", choices=["separate", "merged"],
+                    help="offsets and masks as two tensors, or as DCNv4's one offset/mask tensor")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-stages", action="store_true", help="skip the T-stage images/s sweep")
@@ -385,7 +422,7 @@ def main():
     torch.cuda.set_device(dev)
 
     w = WORKLOADS[args.workload]
-    case = Case(w, dev, rank)
+    case = Case(w, dev, rank, args.layout)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
@@ -411,7 +448,7 @@ def main():
     bwd_ms = statistics.mean(t["bwd"])
     step_ms, fwd_ms, bwd_ms = max_over_ranks([fwd_ms + bwd_ms, fwd_ms, bwd_ms], dist, dev)
 
-    ib = ideal_bytes(w)
+    ib = case.ideal()
     step_bytes = ib["fwd"] + ib["bwd"]
     value = aggregate_gbs(step_bytes, world, step_ms)
 
@@ -431,12 +468,12 @@ def main():
     roof = {
         "bwd": {"bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(bwd_gbs / peak, 4),
-                "traffic": traffic_for(f"bwd@{w.name}", "dcn_bwd.cu"),
+                "traffic": traffic_for(f"bwd@{w.name}", "dcn_bwd.cu") if args.layout == "separate" else None,
                 "phase": "dcn_core_bwd: workspace memset + bwd_kernel + round_kernel",
                 "ms": round(bwd_ms, 5), "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "fwd": {"bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(fwd_gbs / peak, 4),
-                "traffic": traffic_for(f"fwd@{w.name}", "dcn_fwd.cu"),
+                "traffic": traffic_for(f"fwd@{w.name}", "dcn_fwd.cu") if args.layout == "separate" else None,
                 "phase": "dcn_core_fwd: fwd_kernel", "ms": round(fwd_ms, 5),
                 "peak_source": f"{peak_kind} HBM copy bandwidth"},
     }
@@ -445,7 +482,7 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": config_of(w, world),
+        "data": "synthetic", "config": {**config_of(w, world), "layout": args.layout},
         "roofline": {**roof[dominant], "kernel": dominant},
         "roofline_fwd": roof["fwd"],
         "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),

@@ -96,6 +96,7 @@ void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
   kp->os_off = 2 * g.P;
   kp->os_mask = g.P;
   kp->merged = 0;
+  kp->merged_rows64 = 0;
   kp->div_G = fast_div((uint32_t)p->G);
   kp->div_Wo = fast_div((uint32_t)g.Wo);
   kp->div_Ho = fast_div((uint32_t)g.Ho);
@@ -317,6 +318,8 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   if (row_stride) {
     kp.os_off = kp.os_mask = row_stride;
     kp.merged = 1;
+    kp.merged_rows64 = g.P == 9 && es == 2 && aligned(offset, 32) &&
+                       (row_stride * es) % 32 == 0 && env_int("DCN_FWD_ROW64", 1);
   }
   const int cpt = pick_fwd_cpt(p, g, input, output);
   if (cpt < 0) plan_fwd_tiles(p, g, -cpt, &kp);

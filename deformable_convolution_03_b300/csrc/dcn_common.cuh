@@ -44,6 +44,10 @@ struct KParams {
   // (mask = offset + 2P) when merged != 0, whose gradient rows then also get
   // their padding (elements 3P .. stride-1) written as zero.
   int os_off, os_mask, merged;
+  // merged rows that start 32-byte aligned, 16-bit storage, P = 9: the wide
+  // forward reads the first 64 bytes of a row (2P offsets, then P masks) with
+  // two 256-bit loads instead of one load per value
+  int merged_rows64;
   // Kernel taps of the P points, in point order (x-major, centre removed when
   // asked): ix*dilation_w - cen_w and iy*dilation_h - cen_h, as floats (exact).
   float tap_x[DCN_MAX_POINTS];

@@ -173,11 +173,37 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
 #pragma unroll
   for (int i = 0; i < CPT; ++i) acc[i] = 0.f;
 
+  // merged rows of P = 9 in 16-bit storage: the whole row in 16 registers
+  constexpr bool kRow64 = KP == 9 && sizeof(T) == 2;
+  uint32_t row[kRow64 ? 16 : 1];
+  const bool row64 = kRow64 && kp.merged_rows64;
+  if constexpr (kRow64) {
+    if (row64) {
+      uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(row);
+      ldg_words<16>(orow, r16);
+    }
+  }
+
 #pragma unroll(KP > 0 ? KP : 3)
   for (int p = 0; p < P; ++p) {
-    float m = ld_once_1(mrow + p);
+    float m;
+    float2 d;
+    if (kRow64 && row64) {
+      // word p holds (dx, dy) of point p; mask p is half 18 + p
+      uint32_t dw = row[kRow64 ? p : 0];
+      uint32_t mw = row[kRow64 ? (18 + p) / 2 : 0];
+      if constexpr (sizeof(T) == 2) {
+        float lo[2], hi[2];
+        Dt<T>::unpack(dw, lo);
+        Dt<T>::unpack(mw, hi);
+        d = make_float2(lo[0], lo[1]);
+        m = hi[(18 + p) & 1];
+      }
+    } else {
+      m = ld_once_1(mrow + p);
+      d = ld_once_2(orow + 2 * p);
+    }
     if (kp.softmax) m = expf(m - mx) * inv;
-    const float2 d = ld_once_2(orow + 2 * p);
     float x = location(d.x, kp.tap_x[p], scale, ref_x);
     float y = location(d.y, kp.tap_y[p], scale, ref_y);
     if (!in_box(x, y, kp.W, kp.H)) {  // also NaN / inf: every corner falls outside
