@@ -308,8 +308,9 @@ static cudaError_t launch_window_t(const KParams& kp, const WinGeom& wg, const T
   if constexpr (bytes >= 16 && bytes <= 64) {
     const size_t smem = window_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
     auto k9 = bwd_window_kernel<T, CPT, 9>;
+    auto k8 = bwd_window_kernel<T, CPT, 8>;
     auto k0 = bwd_window_kernel<T, CPT, 0>;
-    auto k = kp.P == 9 ? k9 : k0;
+    auto k = kp.P == 9 ? k9 : kp.P == 8 ? k8 : k0;
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem);

@@ -239,8 +239,12 @@ static void launch_wide(const KParams& kp, unsigned grid, int block, cudaStream_
                         const T* o_, const T* m_, T* y_) {
   constexpr int bytes = CPT * (int)sizeof(T);
   if constexpr (bytes >= 16 && bytes <= 64) {
+    // compile-time point counts (fully unrolled) for the 3x3 kernel with and
+    // without its centre; any other count takes the runtime loop
     if (kp.P == 9)
       fwd_wide_kernel<T, CPT, 9><<<grid, block, 0, s>>>(kp, i_, o_, m_, y_);
+    else if (kp.P == 8)
+      fwd_wide_kernel<T, CPT, 8><<<grid, block, 0, s>>>(kp, i_, o_, m_, y_);
     else
       fwd_wide_kernel<T, CPT, 0><<<grid, block, 0, s>>>(kp, i_, o_, m_, y_);
   }
