@@ -3,6 +3,7 @@
 //
 // Every check runs on the host before the first CUDA call, so a rejected
 // call leaves the device untouched.  No entry point allocates memory.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -272,6 +273,85 @@ int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const 
   return 0;
 }
 
+// The split backward: a sample kernel shaped like the wide forward (same
+// channels per thread and tiles, chosen here into *kp) and an input kernel
+// over windows, one thread per output pixel of a TH x TW <= 256 tile of one
+// (image, group).  Of the tile shapes, the one with the least work (tiles x
+// (256 threads + window pixels)) is taken; the window is the tile's footprint
+// plus a halo of R pixels for the offsets, R from 6 (DCN_BWD_HALO) down to 1
+// so that the shared memory stays within kSplitSmem (four CTAs per SM).
+// Needs gc*es of 16, 32 or 64 bytes, P <= 16, grad_out 32-byte aligned (16 for
+// 16-byte rows) and the float32 accumulator 16-byte aligned.  Returns the
+// sample kernel's channels per thread with *wg, *la, *lb filled, or 0.
+//
+// Used by default for 16-bit storage, where it measured fastest on B300
+// (FlashInternImage-T stage 1, fp16: 308 us against 436 us for the
+// single-pass kernel; InternImage-G stage 1, bf16: 391 us against 539 us for
+// the fused window kernel).  For float32 the corner gathers of the sample
+// kernel cost twice as much and the single-pass or window kernels win
+// (64 x 28^2 x 128: 348 us against 227 us).  DCN_BWD_SPLIT=1 uses it for every
+// dtype it can take, 0 never.
+constexpr size_t kSplitSmem = 56 * 1024;
+constexpr size_t kStageSmem = 32 * 1024;
+
+int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const void* gout,
+               const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb) {
+  const int mode = env_int("DCN_BWD_SPLIT", 2);
+  if (mode == 0 || (mode != 1 && p->dtype == DCN_F32)) return 0;
+  const int es = elem_size(p->dtype);
+  const int row = p->gc * es;
+  if ((row != 16 && row != 32 && row != 64) || g.P > 16 || !aligned(acc, 16)) return 0;
+  if (!aligned(gout, row >= 32 ? 32 : 16)) return 0;
+  // the sample kernel: the wide forward's conditions, on input and grad_out
+  const int cpt = -pick_fwd_cpt(p, g, in, gout);
+  if (cpt <= 0) return 0;
+  const int chunks = p->gc / cpt;
+  if (chunks > 32 || (chunks & (chunks - 1))) return 0;
+  // the input kernel's tile and window
+  const double os = p->offset_scale;
+  const int cw = p->dilation_w * (p->kernel_w - 1) / 2, ch = p->dilation_h * (p->kernel_h - 1) / 2;
+  const double x0 = -cw * os, x1 = ((p->kernel_w - 1) * p->dilation_w - cw) * os;
+  const double y0 = -ch * os, y1 = ((p->kernel_h - 1) * p->dilation_h - ch) * os;
+  const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
+  const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
+  const int R0 = env_int("DCN_BWD_HALO", 6);
+  long long best = -1;
+  for (int TW = 1; TW <= 256 && TW <= g.Wo; ++TW) {
+    const int TH = std::min(g.Ho, 256 / TW);
+    dcn::WinGeom c;
+    c.TH = TH;
+    c.TW = TW;
+    c.tiles_h = (g.Ho + TH - 1) / TH;
+    c.tiles_w = (g.Wo + TW - 1) / TW;
+    for (int R = R0; R >= 1; --R) {
+      c.WH = (TH - 1) * p->stride_h + (tmax_y - tmin_y) + 2 * R + 2;
+      c.WW = (TW - 1) * p->stride_w + (tmax_x - tmin_x) + 2 * R + 2;
+      c.org_y = -p->pad_h + ch + tmin_y - R;
+      c.org_x = -p->pad_w + cw + tmin_x - R;
+      if (dcn::split_smem_bytes(c, g.P, p->gc, es) <= kSplitSmem) break;
+    }
+    if (dcn::split_smem_bytes(c, g.P, p->gc, es) > kSplitSmem) continue;
+    const long long cost = (long long)c.tiles_h * c.tiles_w * (256 + (long long)c.WH * c.WW);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *wg = c;
+    }
+  }
+  if (best < 0 || (long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
+  plan_fwd_tiles(p, g, cpt, kp);
+  // grad_offset / grad_mask rows staged in shared memory
+  const int ub = 256 / chunks;
+  if (kp->merged) {
+    *la = kp->os_off;
+    *lb = 0;
+  } else {
+    *la = 2 * g.P;
+    *lb = g.P;
+  }
+  if (!env_int("DCN_BWD_STAGE", 1) || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
+  return cpt;
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCN_OK : DCN_ERR_CUDA; }
 
 }  // namespace
@@ -388,14 +468,20 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
     kp.merged = 1;
   }
   dcn::WinGeom wg;
-  const int wcpt = plan_window(p, g, input, grad_out, acc, &wg);
-  const int cpt = wcpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
+  int la = 0, lb = 0;
+  const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb);
+  const int wcpt = scpt ? 0 : plan_window(p, g, input, grad_out, acc, &wg);
+  const int cpt = scpt || wcpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
   if (fault_injected()) return DCN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (g.n_in > 0) {
     cudaError_t e = cudaMemsetAsync(acc, 0, acc_bytes, s);
     if (e != cudaSuccess) return DCN_ERR_CUDA;
   }
+  if (scpt)
+    return cuda_status(dcn::launch_bwd_split(kp, wg, p->dtype, scpt, la, lb, grad_out, input,
+                                             offset, mask, acc, grad_input, grad_offset,
+                                             grad_mask, s));
   if (wcpt)
     return cuda_status(dcn::launch_bwd_window(kp, wg, p->dtype, wcpt, grad_out, input, offset,
                                               mask, acc, grad_input, grad_offset, grad_mask, s));

@@ -52,20 +52,20 @@ __device__ __forceinline__ void softmax_stats_b(const T* row, int P, float& mx, 
 }
 
 // Atomic float32 add of CPT consecutive values; the address is 16-byte aligned
-// when CPT is a multiple of 4 and 8-byte aligned when it is even.
+// when CPT is a multiple of 4 and 8-byte aligned when it is even.  No kernel
+// reads the accumulator it reduces into, so the reductions carry no memory
+// clobber: the compiler may issue later loads ahead of them.
 template <int CPT>
 __device__ __forceinline__ void red_add(float* dst, const float (&v)[CPT]) {
   if constexpr (CPT % 4 == 0) {
 #pragma unroll
     for (int i = 0; i < CPT; i += 4)
       asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i), "f"(v[i]),
-                   "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3])
-                   : "memory");
+                   "f"(v[i + 1]), "f"(v[i + 2]), "f"(v[i + 3]));
   } else if constexpr (CPT % 2 == 0) {
 #pragma unroll
     for (int i = 0; i < CPT; i += 2)
-      asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(dst + i), "f"(v[i]), "f"(v[i + 1])
-                   : "memory");
+      asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(dst + i), "f"(v[i]), "f"(v[i + 1]));
   } else {
 #pragma unroll
     for (int i = 0; i < CPT; ++i) atomicAdd(dst + i, v[i]);

@@ -213,8 +213,7 @@ bwd_window_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout
           for (int i = 0; i < CPT; i += 4)
             asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i),
                          "f"(w[k] * gof[i]), "f"(w[k] * gof[i + 1]), "f"(w[k] * gof[i + 2]),
-                         "f"(w[k] * gof[i + 3])
-                         : "memory");
+                         "f"(w[k] * gof[i + 3]));
         }
       }
     }
@@ -295,8 +294,7 @@ bwd_window_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout
 #pragma unroll
     for (int k = 0; k < CPT; k += 4)
       asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + k), "f"(acc[k]),
-                   "f"(acc[k + 1]), "f"(acc[k + 2]), "f"(acc[k + 3])
-                   : "memory");
+                   "f"(acc[k + 1]), "f"(acc[k + 2]), "f"(acc[k + 3]));
   }
 }
 

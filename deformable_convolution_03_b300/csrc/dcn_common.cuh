@@ -74,6 +74,19 @@ __host__ __device__ inline size_t window_smem_bytes(const WinGeom& wg, int P, in
   return nsamp * 16 + nunit * gc * es + (3 * ncell + 1) * sizeof(int);
 }
 
+// Shared memory of bwd_input_kernel: per sample (TH*TW*P) its four corner
+// weights (4 x 16 bits for 16-bit storage, 4 x float32 otherwise) and a 16-bit
+// sample id in cell order, the tile's grad_out (gc*es bytes per output
+// pixel), per-cell counts and list heads ((WH-1)*(WW-1) cells), and 32
+// per-warp sums for the scan.
+__host__ __device__ inline size_t split_smem_bytes(const WinGeom& wg, int P, int gc, int es) {
+  const size_t nunit = (size_t)wg.TH * wg.TW, nsamp = nunit * P;
+  const size_t ncell = (size_t)(wg.WH - 1) * (wg.WW - 1);
+  auto up16 = [](size_t b) { return (b + 15) / 16 * 16; };
+  return up16(nsamp * (es == 2 ? 8 : 16)) + up16(nsamp * 2) + nunit * gc * es +
+         (2 * ncell + 1 + 32) * sizeof(int);
+}
+
 // ---- storage dtype traits ---------------------------------------------------
 
 template <typename T> struct Dt;
@@ -236,6 +249,91 @@ __device__ __forceinline__ void ldg_words(const void* p, uint32_t (&w)[NW]) {
     }
   }
 }
+
+// N consecutive 32-bit words starting at the 4-byte aligned address p, read
+// with NV 16-byte loads of the aligned window around them (not kept in L1)
+// and shifted into place in registers.  The caller guarantees that the window
+// [p & ~15, (p & ~15) + 16*NV) lies inside the tensor; 16*NV >= 4*N + 12.
+template <int NV, int N>
+__device__ __forceinline__ void words_from_window(const void* p, uint32_t (&out)[N]) {
+  static_assert(16 * NV >= 4 * N + 12, "window too small");
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const char* base = reinterpret_cast<const char*>(a & ~uintptr_t(15));
+  const int sh = (int)(a & 15) >> 2;  // words to skip, 0..3
+  uint32_t w[4 * NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    asm("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+        : "l"(base + 16 * i));
+#pragma unroll
+  for (int j = 0; j + 2 < 4 * NV; ++j) w[j] = (sh & 2) ? w[j + 2] : w[j];
+#pragma unroll
+  for (int j = 0; j < N; ++j) out[j] = (sh & 1) ? w[j + 1] : w[j];
+}
+
+// The offset row (2P values) and mask row (P values) of one unit in separate
+// tensors, for P = KP fixed at compile time, read with a few 16-byte loads of
+// the aligned windows around them (words_from_window) instead of one scalar
+// load per value.  A warp's lanes hold units whose rows are 2P*es bytes or
+// more apart, so each scalar load instruction would touch up to 32 lines.
+// load() declines (returns false) when a window would leave its tensor (the
+// first or last units of a tensor that is not 16-byte aligned at both ends);
+// the caller then reads the values one by one.
+template <typename T, int KP>
+struct UnitRows {
+  static constexpr int kEs = (int)sizeof(T);
+  static constexpr int kP = KP > 0 ? KP : 1;
+  // offsets: KP words of (dx, dy) 16-bit pairs, or 2*KP float32 words
+  static constexpr int NO = kEs == 2 ? kP : 2 * kP;
+  static constexpr int NVO = (4 * NO + 12 + 15) / 16;
+  // mask: 16-bit values two to a word (value p in half p after the shift),
+  // or one float32 per word
+  static constexpr int NM = kEs == 2 ? (kP + 2) / 2 : kP;
+  static constexpr int NVM = (4 * NM + 12 + 15) / 16;
+  uint32_t ow[NO], mw[NM];
+
+  __device__ __forceinline__ bool load(const T* offset, const T* mask, long long units,
+                                       const T* orow, const T* mrow) {
+    const uintptr_t ob = reinterpret_cast<uintptr_t>(offset);
+    const uintptr_t mb = reinterpret_cast<uintptr_t>(mask);
+    const uintptr_t oe = ob + (uintptr_t)units * 2 * kP * kEs;
+    const uintptr_t me = mb + (uintptr_t)units * kP * kEs;
+    const uintptr_t oa = reinterpret_cast<uintptr_t>(orow) & ~uintptr_t(15);
+    const uintptr_t mw4 = reinterpret_cast<uintptr_t>(mrow) & ~uintptr_t(3);
+    const uintptr_t ma = mw4 & ~uintptr_t(15);
+    if (oa < ob || oa + 16 * NVO > oe || ma < mb || ma + 16 * NVM > me) return false;
+    words_from_window<NVO, NO>(orow, ow);
+    words_from_window<NVM, NM>(reinterpret_cast<const void*>(mw4), mw);
+    if constexpr (kEs == 2) {
+      // the row starts in the upper half of its first word: shift by a half
+      if (reinterpret_cast<uintptr_t>(mrow) & 2) {
+#pragma unroll
+        for (int i = 0; i < NM; ++i)
+          mw[i] = __funnelshift_r(mw[i], i + 1 < NM ? mw[i + 1] : 0u, 16);
+      }
+    }
+    return true;
+  }
+  __device__ __forceinline__ float2 off(int p) const {
+    if constexpr (kEs == 2) {
+      float f[2];
+      Dt<T>::unpack(ow[p], f);
+      return make_float2(f[0], f[1]);
+    } else {
+      return make_float2(__uint_as_float(ow[2 * p]), __uint_as_float(ow[2 * p + 1]));
+    }
+  }
+  __device__ __forceinline__ float msk(int p) const {
+    if constexpr (kEs == 2) {
+      float f[2];
+      Dt<T>::unpack(mw[p >> 1], f);
+      return f[p & 1];
+    } else {
+      return __uint_as_float(mw[p]);
+    }
+  }
+};
 
 // acc[0..2*NW) += weight * (the 16-bit or 32-bit elements packed in w), one
 // product per element, accumulated in float32.  16-bit storage: the weight is

@@ -159,14 +159,31 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
   const float ref_y = (float)(ho * kp.stride_h - kp.pad_h + kp.cen_h);
   const float scale = kp.offset_scale;
 
+  // separate offset / mask tensors and a compile-time point count: the rows
+  // with a few aligned vector loads
+  UnitRows<T, KP> rows;
+  bool vec = false;
+  // (not for 64-byte float32 slices, whose corners already fill the registers)
+  constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
+  if constexpr (kVecRows) vec = !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
+
   // DCNv3: softmax statistics of the unit's logits
   float mx = 0.f, inv = 1.f;
   if (kp.softmax) {
     mx = -INFINITY;
-    for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
-    float s = 0.f;
-    for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
-    inv = 1.f / s;
+    if (vec) {
+#pragma unroll
+      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) mx = fmaxf(mx, rows.msk(p));
+      float s = 0.f;
+#pragma unroll
+      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) s += expf(rows.msk(p) - mx);
+      inv = 1.f / s;
+    } else {
+      for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
+      float s = 0.f;
+      for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
+      inv = 1.f / s;
+    }
   }
 
   float acc[CPT];
@@ -199,6 +216,9 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
         d = make_float2(lo[0], lo[1]);
         m = hi[(18 + p) & 1];
       }
+    } else if (KP > 0 && vec) {
+      m = rows.msk(KP > 0 ? p : 0);
+      d = rows.off(KP > 0 ? p : 0);
     } else {
       m = ld_once_1(mrow + p);
       d = ld_once_2(orow + 2 * p);

@@ -34,4 +34,16 @@ cudaError_t launch_bwd_window(const KParams& kp, const WinGeom& wg, int dtype, i
                               const void* gout, const void* in, const void* off, const void* msk,
                               float* gin_acc, void* gin, void* goff, void* gmask, cudaStream_t s);
 
+// The split backward (dcn_bwd_split.cu): bwd_sample_kernel (grad_offset,
+// grad_mask) with cpt as the wide forward's and the tiles in kp, then
+// bwd_input_kernel (grad_input) over the windows of wg, gc*sizeof(T) of 16,
+// 32 or 64 bytes, P <= 16, TH*TW <= 256.  la, lb: elements per unit of the
+// staged offset and mask rows (0: written straight to memory).  gin_acc
+// (float32) must be cleared by the caller; when it is not gin, it is rounded
+// into gin at the end.
+cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, int cpt, int la,
+                             int lb, const void* gout, const void* in, const void* off,
+                             const void* msk, float* gin_acc, void* gin, void* goff, void* gmask,
+                             cudaStream_t s);
+
 }  // namespace dcn

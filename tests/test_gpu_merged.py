@@ -28,8 +28,19 @@ CASES = [
 ]
 
 
+BWD = {
+    "default": {},
+    "split": {"DCN_BWD_SPLIT": "1"},
+    "single_pass": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "0"},
+}
+
+
+@pytest.mark.parametrize("bwd", list(BWD))
 @pytest.mark.parametrize("name,over,stride", CASES, ids=[c[0] for c in CASES])
-def test_merged_layout_forward_and_backward(name, over, stride):
+def test_merged_layout_forward_and_backward(name, over, stride, bwd, monkeypatch):
+    # every backward path reads the merged rows and writes their padding
+    for k, v in BWD[bwd].items():
+        monkeypatch.setenv(k, v)
     w = WORKLOADS[name].with_(backward=True, **over)
     t = make_inputs(w, grad=True)
     p = lib_params(w)

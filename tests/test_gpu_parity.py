@@ -94,6 +94,7 @@ def test_small_forward_and_backward(w):
 def test_every_general_kernel_instance(dt, cap, monkeypatch):
     # force each channels-per-thread instance of the general kernels
     monkeypatch.setenv("DCN_FWD_WIDE", "0")
+    monkeypatch.setenv("DCN_BWD_SPLIT", "0")
     monkeypatch.setenv("DCN_BWD_WINDOW", "0")
     monkeypatch.setenv("DCN_FWD_CPT", str(cap))
     monkeypatch.setenv("DCN_BWD_CPT", str(cap))
@@ -132,26 +133,38 @@ SPLIT = [
 ]
 
 
+BWD_MODES = {
+    # the split kernels (sample kernel + windowed input kernel), every dtype
+    "split": {"DCN_BWD_SPLIT": "1"},
+    # the same with a one-pixel halo: most samples leave the window and take
+    # the far path
+    "split_halo1": {"DCN_BWD_SPLIT": "1", "DCN_BWD_HALO": "1"},
+    # the split kernels with gradient rows written straight to memory and the
+    # sample kernel over consecutive items instead of tiles
+    "split_direct": {"DCN_BWD_SPLIT": "1", "DCN_BWD_STAGE": "0", "DCN_FWD_TILE": "0"},
+    # the fused windowed kernel, with its default halo and with one pixel
+    "window": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1"},
+    "window_halo1": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1", "DCN_BWD_HALO": "1"},
+    # the single-pass atomic kernels
+    "single_pass": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "0"},
+}
+
+
 @pytest.mark.parametrize("w", SPLIT, ids=lambda w: w.name)
-@pytest.mark.parametrize("mode", ["window", "halo1", "single_pass"])
+@pytest.mark.parametrize("mode", list(BWD_MODES))
 def test_backward_paths(w, mode, monkeypatch):
-    # the windowed kernel, the same with a one-pixel halo (most samples leave
-    # the window and take the far path), and the single-pass atomic kernels
-    if mode in ("window", "halo1"):
-        monkeypatch.setenv("DCN_BWD_WINDOW", "1")
-    if mode == "halo1":
-        monkeypatch.setenv("DCN_BWD_HALO", "1")
-    if mode == "single_pass":
-        monkeypatch.setenv("DCN_BWD_WINDOW", "0")
+    for k, v in BWD_MODES[mode].items():
+        monkeypatch.setenv(k, v)
     check_bwd(w, make_inputs(w))
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("window", ["1", "0"])
-def test_backward_crowded_samples(dt, window, monkeypatch):
+@pytest.mark.parametrize("mode", ["split", "window", "single_pass"])
+def test_backward_crowded_samples(dt, mode, monkeypatch):
     # every sample of a 32x32 image aimed at one cell: the cells inside each
     # tile's window collect hundreds of samples, the rest leave the window
-    monkeypatch.setenv("DCN_BWD_WINDOW", window)
+    for k, v in BWD_MODES[mode].items():
+        monkeypatch.setenv(k, v)
     w = small(f"crowd_{dt}", dt, gc=16, G=1, N=1, H=32, W=32, softmax=1)
     t = make_inputs(w)
     ho = torch.arange(w.H_out).view(-1, 1, 1)
