@@ -301,6 +301,7 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
   const int es = elem_size(p->dtype);
   const int row = p->gc * es;
   if ((row != 16 && row != 32 && row != 64) || g.P > 16 || !aligned(acc, 16)) return 0;
+  if ((long long)p->H * p->W >= (1LL << 31)) return 0;  // pixel offsets in 32 bits
   if (!aligned(gout, row >= 32 ? 32 : 16)) return 0;
   // the sample kernel: the wide forward's conditions, on input and grad_out
   const int cpt = -pick_fwd_cpt(p, g, in, gout);

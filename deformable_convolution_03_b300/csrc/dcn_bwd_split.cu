@@ -31,6 +31,7 @@
 // Corners outside the image read zero, so their d_k is zero and they receive
 // nothing.
 #include <climits>
+#include <cstdlib>
 #include <type_traits>
 
 #include "dcn_common.cuh"
@@ -68,10 +69,12 @@ __device__ __forceinline__ void warp_copy_out(void* dst, const void* src, int by
 // the mask rows; for the merged layout la is the row stride and lb is 0) and
 // written out row by row of the tile with 16-byte stores.
 template <typename T, int CPT, int KP>
-__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2)
-bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ input,
-                  const T* __restrict__ offset, const T* __restrict__ mask,
-                  T* __restrict__ goff, T* __restrict__ gmask, int la, int lb) {
+__device__ __forceinline__ void sample_block(const KParams& kp, const T* __restrict__ gout,
+                                             const T* __restrict__ input,
+                                             const T* __restrict__ offset,
+                                             const T* __restrict__ mask, T* __restrict__ goff,
+                                             T* __restrict__ gmask, int la, int lb,
+                                             const unsigned bid) {
   constexpr int NW = CPT * (int)sizeof(T) / 4;
   extern __shared__ __align__(16) unsigned char smem[];
   const int chunks = kp.gc / CPT;
@@ -86,8 +89,8 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
     g = r / chunks;
     c0 = (r - g * chunks) * CPT;
     const int tiles = kp.tiles_w * kp.tiles_h;
-    n = blockIdx.x / tiles;
-    const int t = blockIdx.x - n * tiles;
+    n = bid / tiles;
+    const int t = bid - n * tiles;
     const int ty = t / kp.tiles_w;
     ho0 = ty * kp.tile_h;
     wo0 = (t - ty * kp.tiles_w) * kp.tile_w;
@@ -96,7 +99,7 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
     active = lp < kp.tile_w * kp.tile_h && ho < kp.Ho && wo < kp.Wo;
     if (active) unit = ((n * (uint32_t)kp.Ho + ho) * kp.Wo + wo) * kp.G + g;
   } else {
-    const uint32_t item = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t item = bid * blockDim.x + threadIdx.x;
     active = item < (uint32_t)(kp.units * chunks);
     const uint32_t it = active ? item : 0;
     unit = chunks == 1 ? it : it / (uint32_t)chunks;
@@ -263,7 +266,7 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
         warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * la + l0 * lb, cnt * lb * es, lane);
     }
   } else {
-    const long long u0 = (long long)blockIdx.x * ub;
+    const long long u0 = (long long)bid * ub;
     const int cnt = (int)min((long long)ub, kp.units - u0);
     if (cnt > 0 && warp == 0) {
       warp_copy_out(goff + u0 * kp.os_off, s_rows, cnt * la * es, lane);
@@ -272,6 +275,15 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
     }
   }
 }
+
+template <typename T, int CPT, int KP>
+__global__ void __launch_bounds__(256, sizeof(T) == 2 ? 3 : 2)
+bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ input,
+                  const T* __restrict__ offset, const T* __restrict__ mask,
+                  T* __restrict__ goff, T* __restrict__ gmask, int la, int lb) {
+  sample_block<T, CPT, KP>(kp, gout, input, offset, mask, goff, gmask, la, lb, blockIdx.x);
+}
+
 
 // ---- the input half ---------------------------------------------------------
 // A CTA owns TH x TW <= blockDim.x output pixels of one (image, group); a
@@ -297,10 +309,11 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
 // the storage type once and multiplied exactly into the float32 sum
 // (mixed-precision FMA), as in the forward.
 template <typename T, int NW, int KP>
-__global__ void __launch_bounds__(256, NW <= 8 ? 4 : 2)
-bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
-                 const T* __restrict__ offset, const T* __restrict__ mask,
-                 float* __restrict__ gin) {
+__device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg,
+                                            const T* __restrict__ gout,
+                                            const T* __restrict__ offset,
+                                            const T* __restrict__ mask, float* __restrict__ gin,
+                                            const unsigned bid) {
   constexpr int CPT = NW * 4 / (int)sizeof(T);  // = gc
   constexpr int KPN = KP > 0 ? KP : 16;
   constexpr bool k16 = sizeof(T) == 2;
@@ -323,8 +336,8 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
 
   // block = (image, tile, group) with the group fastest, so that the CTAs of
   // one tile read neighbouring sectors of the same lines at about one time
-  const int g = blockIdx.x % kp.G;
-  const int rest = blockIdx.x / kp.G;
+  const int g = bid % kp.G;
+  const int rest = bid / kp.G;
   const int tiles = wg.tiles_h * wg.tiles_w;
   const int t = rest % tiles, n = rest / tiles;
   const int th = t / wg.tiles_w, tw = t - th * wg.tiles_w;
@@ -504,13 +517,22 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
   __syncthreads();
 
   // ---- pass 3: per window pixel inside the image --------------------------
+  // Warps take 32 consecutive pixels of the window (clipped to the image).
+  // Afterwards each group of L = gc/4 lanes transposes its float4 chunks, so
+  // that the group's lanes reduce the L chunks of one pixel side by side:
+  // one vector reduction instruction then covers 32/L pixels' contiguous
+  // slices instead of 32 scattered 16-byte pieces.
+  constexpr int L = CPT / 4;
+  const int lane = threadIdx.x & 31;
   const int ry0 = max(0, -wy0), ry1 = min(wg.WH, H - wy0);
   const int rx0 = max(0, -wx0), rx1 = min(wg.WW, W - wx0);
   const int cols = rx1 - rx0;
   const int npix = cols > 0 && ry1 > ry0 ? (ry1 - ry0) * cols : 0;
-  for (int i = threadIdx.x; i < npix; i += blockDim.x) {
-    const int qy = i / cols;
-    const int ry = ry0 + qy, rx = rx0 + (i - qy * cols);
+  for (int base = threadIdx.x - lane; base < npix; base += blockDim.x) {
+    const int i = base + lane;
+    const bool valid = i < npix;
+    const int qy = valid ? i / cols : 0;
+    const int ry = ry0 + qy, rx = rx0 + (valid ? i - qy * cols : 0);
     const int yy = wy0 + ry, xx = wx0 + rx;
     // the cells (cy, rx - 1) and (cy, rx) of cell rows cy = ry - 1 (range a,
     // the pixel is their lower corner) and cy = ry (range b, upper corner):
@@ -518,20 +540,19 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
     // cell rx; cells outside the window's grid are empty
     int sa = 0, ma = 0, ea = 0, sb = 0, mb = 0, eb = 0;
     const int lo = max(rx - 1, 0), hi = min(rx + 1, cw);
-    if (ry >= 1) {
-      const int base = (ry - 1) * cw;
-      sa = head[base + lo];
-      ma = head[base + rx];
-      ea = head[base + hi];
+    if (valid && ry >= 1) {
+      const int cb = (ry - 1) * cw;
+      sa = head[cb + lo];
+      ma = head[cb + rx];
+      ea = head[cb + hi];
     }
-    if (ry < wg.WH - 1) {
-      const int base = ry * cw;
-      sb = head[base + lo];
-      mb = head[base + rx];
-      eb = head[base + hi];
+    if (valid && ry < wg.WH - 1) {
+      const int cb = ry * cw;
+      sb = head[cb + lo];
+      mb = head[cb + rx];
+      eb = head[cb + hi];
     }
     const int na = ea - sa, nv = na + (eb - sb);
-    if (nv == 0) continue;
     float acc[CPT];
 #pragma unroll
     for (int k = 0; k < CPT; ++k) acc[k] = 0.f;
@@ -582,13 +603,75 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
       row(u0, r0);
       fma_words<T, NW>(acc, r0, w0);
     }
-    float* dst = gin + img_off + ((size_t)yy * W + xx) * kp.C;
+    // lane j of a group holds chunks 0..L-1 of its own pixel; after the
+    // transpose it holds chunk j of the group's pixels 0..L-1
+    const int j = lane & (L - 1);
 #pragma unroll
-    for (int k = 0; k < CPT; k += 4)
-      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + k), "f"(acc[k]),
-                   "f"(acc[k + 1]), "f"(acc[k + 2]), "f"(acc[k + 3]));
+    for (int sb2 = 1; sb2 < L; sb2 <<= 1) {
+#pragma unroll
+      for (int t = 0; t < L; ++t) {
+        if (t & sb2) continue;
+        const bool hi_lane = (j & sb2) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float send = hi_lane ? acc[4 * t + e] : acc[4 * (t | sb2) + e];
+          const float got = __shfl_xor_sync(0xffffffffu, send, sb2);
+          if (hi_lane)
+            acc[4 * t + e] = got;
+          else
+            acc[4 * (t | sb2) + e] = got;
+        }
+      }
+    }
+    const unsigned got_any = __ballot_sync(0xffffffffu, nv > 0);
+    const int pix_off = valid ? yy * W + xx : 0;
+    const int g0 = lane & ~(L - 1);
+#pragma unroll
+    for (int r = 0; r < L; ++r) {
+      const int off = __shfl_sync(0xffffffffu, pix_off, g0 + r);
+      if (!((got_any >> (g0 + r)) & 1u)) continue;
+      float* dst = gin + img_off + (size_t)off * kp.C + 4 * j;
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[4 * r]),
+                   "f"(acc[4 * r + 1]), "f"(acc[4 * r + 2]), "f"(acc[4 * r + 3]));
+    }
   }
 }
+
+template <typename T, int NW, int KP>
+__global__ void __launch_bounds__(256, NW <= 8 ? 4 : 2)
+bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
+                 const T* __restrict__ offset, const T* __restrict__ mask,
+                 float* __restrict__ gin) {
+  input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, blockIdx.x);
+}
+
+// Both halves in one launch: their blocks interleaved one to one (then the
+// rest of the longer list), so that every SM runs gather-bound sample blocks
+// and shared-memory-bound input blocks side by side instead of one kind after
+// the other.  The two halves share no data: the sample half writes grad_offset
+// and grad_mask, the input half reduces into the cleared accumulator.
+template <typename T, int CPT, int NW, int KP>
+__global__ void __launch_bounds__(256, 3)
+bwd_both_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
+                const T* __restrict__ input, const T* __restrict__ offset,
+                const T* __restrict__ mask, T* __restrict__ goff, T* __restrict__ gmask, int la,
+                int lb, float* __restrict__ gin, unsigned n_sample, unsigned n_input) {
+  const unsigned b = blockIdx.x, m = min(n_sample, n_input);
+  bool sample;
+  unsigned id;
+  if (b < 2 * m) {
+    sample = (b & 1) == 0;
+    id = b >> 1;
+  } else {
+    sample = n_sample > n_input;
+    id = b - m;
+  }
+  if (sample)
+    sample_block<T, CPT, KP>(kp, gout, input, offset, mask, goff, gmask, la, lb, id);
+  else
+    input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, id);
+}
+
 
 // ---- launches ----------------------------------------------------------------
 
@@ -642,6 +725,33 @@ static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T*
   return cudaGetLastError();
 }
 
+// Both halves as one launch of bwd_both_kernel (DCN_BWD_FUSE=0: two launches).
+template <typename T, int CPT, int NW>
+static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* go_, const T* i_,
+                                 const T* o_, const T* m_, T* goff_, T* gm_, int la, int lb,
+                                 float* acc, cudaStream_t s) {
+  const int chunks = kp.gc / CPT;
+  const int block = 256;
+  const long long na = kp.tile_w > 0 ? (long long)kp.N * kp.tiles_w * kp.tiles_h
+                                     : (kp.units * chunks + block - 1) / block;
+  const long long nb = (long long)kp.N * kp.G * wg.tiles_h * wg.tiles_w;
+  if (na + nb > INT_MAX) return cudaErrorInvalidConfiguration;
+  const size_t sa = la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0;
+  const size_t sb = split_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
+  const size_t smem = sa > sb ? sa : sb;
+  auto k9 = bwd_both_kernel<T, CPT, NW, 9>;
+  auto k8 = bwd_both_kernel<T, CPT, NW, 8>;
+  auto k0 = bwd_both_kernel<T, CPT, NW, 0>;
+  auto k = kp.P == 9 ? k9 : kp.P == 8 ? k8 : k0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k<<<(unsigned)(na + nb), block, smem, s>>>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc,
+                                             (unsigned)na, (unsigned)nb);
+  return cudaGetLastError();
+}
+
 template <typename T>
 static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, int la, int lb,
                                 const void* gout, const void* in, const void* off, const void* msk,
@@ -653,6 +763,36 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
   T* goff_ = static_cast<T*>(goff);
   T* gm_ = static_cast<T*>(gmask);
   cudaError_t e;
+  const int nw = kp.gc * (int)sizeof(T) / 4;
+  const char* fuse = std::getenv("DCN_BWD_FUSE");
+  if (!(fuse && fuse[0] == '0')) {
+    // the (channels per sample thread, words per unit row) pairs that occur
+    if constexpr (sizeof(T) == 2) {
+      if (cpt == 8 && nw == 4)
+        e = launch_both_t<T, 8, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else if (cpt == 16 && nw == 8)
+        e = launch_both_t<T, 16, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else if (cpt == 16 && nw == 16)
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else
+        return cudaErrorInvalidValue;
+    } else {
+      if (cpt == 4 && nw == 4)
+        e = launch_both_t<T, 4, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else if (cpt == 8 && nw == 8)
+        e = launch_both_t<T, 8, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else if (cpt == 16 && nw == 16)
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+      else
+        return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    if ((void*)acc != gin) {
+      const int dt = std::is_same<T, __half>::value ? DCN_F16 : DCN_BF16;
+      return launch_round(dt, acc, gin, (long long)kp.N * kp.H * kp.W * kp.C, s);
+    }
+    return cudaSuccess;
+  }
   switch (cpt) {
     case 4: e = launch_sample_t<T, 4>(kp, go_, i_, o_, m_, goff_, gm_, la, lb, s); break;
     case 8: e = launch_sample_t<T, 8>(kp, go_, i_, o_, m_, goff_, gm_, la, lb, s); break;
@@ -660,7 +800,7 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  switch (kp.gc * (int)sizeof(T) / 4) {
+  switch (nw) {
     case 4: e = launch_input_t<T, 4>(kp, wg, go_, o_, m_, acc, s); break;
     case 8: e = launch_input_t<T, 8>(kp, wg, go_, o_, m_, acc, s); break;
     case 16: e = launch_input_t<T, 16>(kp, wg, go_, o_, m_, acc, s); break;

@@ -142,6 +142,8 @@ BWD_MODES = {
     # the split kernels with gradient rows written straight to memory and the
     # sample kernel over consecutive items instead of tiles
     "split_direct": {"DCN_BWD_SPLIT": "1", "DCN_BWD_STAGE": "0", "DCN_FWD_TILE": "0"},
+    # the two split kernels as separate launches instead of one
+    "split_unfused": {"DCN_BWD_SPLIT": "1", "DCN_BWD_FUSE": "0"},
     # the fused windowed kernel, with its default halo and with one pixel
     "window": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1"},
     "window_halo1": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1", "DCN_BWD_HALO": "1"},
