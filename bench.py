@@ -52,21 +52,26 @@ FALLBACK_HBM_GBS = 6400.0
 # workload, with the sha1 of the kernel source it was taken on: a changed
 # source voids the figure.
 TRAFFIC = {
-    # profiles/fwd_wide_t_stage1_f16.md
-    "fwd@t_stage1_f16": {"bytes": 69_104_384 + 3_520_256, "sha": "819c2d87b4e4"},
-    # profiles/bwd_kernel_t_stage1_f16.md: bwd_kernel + round_kernel (the memset is not a kernel)
-    "bwd@t_stage1_f16": {"bytes": 146_143_232 + 51_331_840 + 51_386_368 + 1_508_864, "sha": "ceb5ed66dbc1"},
+    # profiles/launches_t_stage1_f16.md: fwd_wide_kernel, per launch
+    "fwd@t_stage1_f16": {"bytes": 69_081_767 + 1_295_983, "sha": "8557bc1c4bfa"},
+    # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
+    # call (the accumulator's memset is not a kernel and is not counted)
+    "bwd@t_stage1_f16": {"bytes": 169_838_959 + 44_507_136 + 51_389_184 + 112_506,
+                         "sha": "3dcfb874fec6"},
 }
 
 
-def src_sha(name: str) -> str:
-    path = os.path.join(ROOT, "deformable_convolution_03_b300", "csrc", name)
-    return hashlib.sha1(open(path, "rb").read()).hexdigest()[:12]
+def src_sha(names) -> str:
+    h = hashlib.sha1()
+    for name in names:
+        path = os.path.join(ROOT, "deformable_convolution_03_b300", "csrc", name)
+        h.update(open(path, "rb").read())
+    return h.hexdigest()[:12]
 
 
-def traffic_for(key: str, src: str):
+def traffic_for(key: str, srcs):
     rec = TRAFFIC.get(key)
-    if not rec or rec["sha"] != src_sha(src):
+    if not rec or rec["sha"] != src_sha(srcs):
         return None
     return rec["bytes"]
 
@@ -235,7 +240,8 @@ class Case:
         return ib
 
     def launches_per_step(self) -> int:
-        # forward kernel; backward kernel; the rounding kernel of 16-bit grad_input
+        # forward kernel; backward kernel (both halves in one launch, or the
+        # single-pass kernel for float32); the rounding kernel of 16-bit grad_input
         return 2 + (1 if self.ws_bytes else 0)
 
 
@@ -468,13 +474,13 @@ def main():
     roof = {
         "bwd": {"bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(bwd_gbs / peak, 4),
-                "traffic": traffic_for(f"bwd@{w.name}", "dcn_bwd.cu") if args.layout == "separate" else None,
-                "phase": "dcn_core_bwd: workspace memset + bwd_kernel + round_kernel",
+                "traffic": traffic_for(f"bwd@{w.name}", ("dcn_bwd_split.cu", "dcn_bwd.cu")) if args.layout == "separate" else None,
+                "phase": "dcn_core_bwd: workspace memset + bwd_both_kernel + round_kernel",
                 "ms": round(bwd_ms, 5), "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "fwd": {"bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(fwd_gbs / peak, 4),
-                "traffic": traffic_for(f"fwd@{w.name}", "dcn_fwd.cu") if args.layout == "separate" else None,
-                "phase": "dcn_core_fwd: fwd_kernel", "ms": round(fwd_ms, 5),
+                "traffic": traffic_for(f"fwd@{w.name}", ("dcn_fwd.cu",)) if args.layout == "separate" else None,
+                "phase": "dcn_core_fwd: fwd_wide_kernel", "ms": round(fwd_ms, 5),
                 "peak_source": f"{peak_kind} HBM copy bandwidth"},
     }
 

@@ -317,19 +317,24 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
   constexpr int CPT = NW * 4 / (int)sizeof(T);  // = gc
   constexpr int KPN = KP > 0 ? KP : 16;
   constexpr bool k16 = sizeof(T) == 2;
-  // the four weights of a sample: 4 x 16 bits, or 4 x float32
+  // the four weights of a sample: 4 x 16 bits, or 4 x float32; and the two of
+  // one row of its corners: (x0, x1) as 2 x 16 bits or 2 x float32
   using Wq = typename std::conditional<k16, uint2, float4>::type;
+  using Wh = typename std::conditional<k16, uint32_t, float2>::type;
   extern __shared__ __align__(16) unsigned char smem[];
   const int P = KP > 0 ? KP : kp.P;
   const int nunit = wg.TH * wg.TW;
   const int nsamp = nunit * P;
   const int cw = wg.WW - 1, ncell = (wg.WH - 1) * cw;
   auto up16 = [](int b) { return (b + 15) & ~15; };
-  Wq* ew = reinterpret_cast<Wq*>(smem);                                  // nsamp, by sample
-  unsigned short* ids = reinterpret_cast<unsigned short*>(
-      smem + up16(nsamp * (int)sizeof(Wq)));                             // nsamp, by cell
+  // in cell order: the weights of the corner row y0 + 1 (wa) and y0 (wb), and
+  // the sample's unit in the tile
+  Wh* wa = reinterpret_cast<Wh*>(smem);                                  // nsamp
+  Wh* wb = wa + nsamp;                                                   // nsamp
+  unsigned short* eu = reinterpret_cast<unsigned short*>(
+      smem + up16(nsamp * (int)sizeof(Wq)));                             // nsamp
   uint32_t* gos = reinterpret_cast<uint32_t*>(
-      reinterpret_cast<unsigned char*>(ids) + up16(nsamp * 2));          // nunit * NW
+      reinterpret_cast<unsigned char*>(eu) + up16(nsamp * 2));           // nunit * NW
   int* count = reinterpret_cast<int*>(gos + nunit * NW);                 // ncell
   int* head = count + ncell;                                             // ncell + 1
   int* wsum = head + ncell + 1;                                          // 32
@@ -389,9 +394,10 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
     inv = 1.f / s;
   }
 
-  // per point: (rank << 16) | cell for an in-window sample, else -1; far
-  // samples are marked in a bit mask and done after the loop
+  // per point: (rank << 16) | cell for an in-window sample, else -1, and its
+  // weights; far samples are marked in a bit mask and done after the loop
   int code[KPN];
+  Wq wq[KPN];
   uint32_t far = 0;
   // the unit's offsets and weights, all loads issued before any use
   float2 dd[KPN];
@@ -435,14 +441,12 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
     if ((unsigned)cy < (unsigned)(wg.WH - 1) && (unsigned)cx < (unsigned)cw) {
       const int cell = cy * cw + cx;
       code[p] = (atomicAdd(&count[cell], 1) << 16) | cell;
-      Wq q;
       if constexpr (k16) {
-        q.x = (uint32_t)Fma<T>::weight(w[0]) | ((uint32_t)Fma<T>::weight(w[1]) << 16);
-        q.y = (uint32_t)Fma<T>::weight(w[2]) | ((uint32_t)Fma<T>::weight(w[3]) << 16);
+        wq[p].x = (uint32_t)Fma<T>::weight(w[0]) | ((uint32_t)Fma<T>::weight(w[1]) << 16);
+        wq[p].y = (uint32_t)Fma<T>::weight(w[2]) | ((uint32_t)Fma<T>::weight(w[3]) << 16);
       } else {
-        q = make_float4(w[0], w[1], w[2], w[3]);
+        wq[p] = make_float4(w[0], w[1], w[2], w[3]);
       }
-      ew[local * P + p] = q;
     } else {
       far |= 1u << p;
     }
@@ -512,7 +516,15 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
 #pragma unroll(KP > 0 ? KP : 1)
   for (int p = 0; p < P; ++p) {
     if (code[p] < 0) continue;
-    ids[head[code[p] & 0xffff] + (code[p] >> 16)] = (unsigned short)(local * P + p);
+    const int o = head[code[p] & 0xffff] + (code[p] >> 16);
+    if constexpr (k16) {
+      wa[o] = wq[p].y;
+      wb[o] = wq[p].x;
+    } else {
+      wa[o] = make_float2(wq[p].z, wq[p].w);
+      wb[o] = make_float2(wq[p].x, wq[p].y);
+    }
+    eu[o] = (unsigned short)local;
   }
   __syncthreads();
 
@@ -561,16 +573,13 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
       const bool in_a = v < na;
       const int o = in_a ? sa + v : sb + (v - na);
       const bool right = o < (in_a ? ma : mb);
-      const int id = ids[o];
-      const Wq q = ew[id];
-      un = id / P;
+      const Wh h = (in_a ? wa : wb)[o];
+      un = eu[o];
+      // the right corner (x1) of the row: the high half, or .y
       if constexpr (k16) {
-        // a: corners (1,0), (1,1) in q.y; b: (0,0), (0,1) in q.x; the right
-        // corner (x1) in the high half
-        const uint32_t word = in_a ? q.y : q.x;
-        return (unsigned short)(right ? word >> 16 : word & 0xffffu);
+        return (unsigned short)(right ? h >> 16 : h & 0xffffu);
       } else {
-        return in_a ? (right ? q.w : q.z) : (right ? q.y : q.x);
+        return right ? h.y : h.x;
       }
     };
     auto row = [&](int un, uint32_t (&vv)[NW]) {
@@ -638,7 +647,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
 }
 
 template <typename T, int NW, int KP>
-__global__ void __launch_bounds__(256, NW <= 8 ? 4 : 2)
+__global__ void __launch_bounds__(256, NW <= 8 ? 3 : 2)
 bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
                  const T* __restrict__ offset, const T* __restrict__ mask,
                  float* __restrict__ gin) {

@@ -74,9 +74,9 @@ __host__ __device__ inline size_t window_smem_bytes(const WinGeom& wg, int P, in
   return nsamp * 16 + nunit * gc * es + (3 * ncell + 1) * sizeof(int);
 }
 
-// Shared memory of bwd_input_kernel: per sample (TH*TW*P) its four corner
-// weights (4 x 16 bits for 16-bit storage, 4 x float32 otherwise) and a 16-bit
-// sample id in cell order, the tile's grad_out (gc*es bytes per output
+// Shared memory of bwd_input_kernel: per sample (TH*TW*P), in cell order, its
+// four corner weights (4 x 16 bits for 16-bit storage, 4 x float32 otherwise)
+// and its 16-bit unit, the tile's grad_out (gc*es bytes per output
 // pixel), per-cell counts and list heads ((WH-1)*(WW-1) cells), and 32
 // per-warp sums for the scan.
 __host__ __device__ inline size_t split_smem_bytes(const WinGeom& wg, int P, int gc, int es) {
