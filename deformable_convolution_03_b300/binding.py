@@ -32,7 +32,7 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
-           "dcn_status_str", "dcn_version")
+           "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -97,6 +97,7 @@ def lib() -> ctypes.CDLL:
         L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
         L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t,
                                       vp]
+        L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -130,6 +131,13 @@ def dcn_status_str(status: int) -> str:
 
 def dcn_version() -> int:
     return int(lib().dcn_version())
+
+
+def dcn_wait_timeouts() -> int:
+    """Blocks whose bounded wait for a tensor copy ran out (current device)."""
+    n = ctypes.c_ulonglong(0)
+    _check(lib().dcn_wait_timeouts(ctypes.byref(n)), "dcn_wait_timeouts")
+    return int(n.value)
 
 
 def dcn_out_shape(p: Params) -> tuple[int, int]:

@@ -192,6 +192,79 @@ void plan_fwd_tiles(const dcn_params_t* p, const Geometry& g, int cpt, dcn::KPar
   kp->tiles_h = (int)tiles_h;
 }
 
+// The TMA-staged forward: the wide forward's slices, GB groups per block
+// (all of them when a pixel's channels fit in 128 bytes, else the largest
+// divisor of G that does), a power-of-two tile of 256 / (GB * gc/cpt) output
+// pixels, and a window of the tile's footprint plus a halo of R pixels, R from
+// 6 (DCN_FWD_HALO) down to 0 so that the window stays within kTileSmem (three
+// blocks per SM).  Needs the input 16-byte aligned and every tensor-map
+// stride a multiple of 16 bytes; fills the tensor map.  DCN_FWD_TMA=0 turns it
+// off.
+constexpr size_t kTileSmem = 64 * 1024;
+
+bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void* in,
+                   dcn::KParams* kp, dcn::TileGeom* tg, void* map) {
+  if (!env_int("DCN_FWD_TMA", 1)) return false;
+  const int es = elem_size(p->dtype);
+  const long long C = (long long)p->G * p->gc;
+  if (!aligned(in, 16) || (C * es) % 16 || (p->gc * es) % 16) return false;
+  if ((long long)p->N * p->H * p->W * C >= (1LL << 40)) return false;
+  int GB = 0;
+  for (int d = p->G; d >= 1; --d)
+    if (p->G % d == 0 && (long long)d * p->gc * es <= 128) {
+      GB = d;
+      break;
+    }
+  if (!GB) return false;
+  const int chunks = p->gc / cpt;
+  const int per_px = GB * chunks;
+  if (per_px > 256 || (per_px & (per_px - 1))) return false;
+  const int px = 256 / per_px;
+  // least-padding power-of-two tile, then the squarest
+  long long best = -1;
+  int bw = 0, bh = 0;
+  for (int tw = 1; tw <= px; tw <<= 1) {
+    const int th = px / tw;
+    const long long padded = (long long)((g.Wo + tw - 1) / tw) * tw * ((g.Ho + th - 1) / th) * th;
+    const int skew = tw > th ? tw / th : th / tw;
+    const int bskew = bw > bh ? (bh ? bw / bh : 0) : (bw ? bh / bw : 0);
+    if (best < 0 || padded < best || (padded == best && skew < bskew)) {
+      best = padded;
+      bw = tw;
+      bh = th;
+    }
+  }
+  if (best * 5 > (long long)g.Wo * g.Ho * 6) return false;  // more than 20 % padding
+  const double os = p->offset_scale;
+  const int cw = p->dilation_w * (p->kernel_w - 1) / 2, ch = p->dilation_h * (p->kernel_h - 1) / 2;
+  const double x0 = -cw * os, x1 = ((p->kernel_w - 1) * p->dilation_w - cw) * os;
+  const double y0 = -ch * os, y1 = ((p->kernel_h - 1) * p->dilation_h - ch) * os;
+  const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
+  const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
+  const size_t rb = (size_t)GB * p->gc * es;
+  for (int R = env_int("DCN_FWD_HALO", 6); R >= 0; --R) {
+    const long long WH = (long long)(bh - 1) * p->stride_h + (tmax_y - tmin_y) + 2 + 2 * R;
+    const long long WW = (long long)(bw - 1) * p->stride_w + (tmax_x - tmin_x) + 2 + 2 * R;
+    if (WH > 256 || WW > 256 || (size_t)(WH * WW) * rb > kTileSmem) continue;
+    tg->GB = GB;
+    tg->ngb = p->G / GB;
+    tg->WH = (int)WH;
+    tg->WW = (int)WW;
+    tg->org_y = -p->pad_h + ch + tmin_y - R;
+    tg->org_x = -p->pad_w + cw + tmin_x - R;
+    tg->win_bytes = (unsigned)(WH * WW * rb);
+    tg->swz = rb == 128 && env_int("DCN_FWD_SWIZZLE", 0);
+    const long long tiles_w = (g.Wo + bw - 1) / bw, tiles_h = (g.Ho + bh - 1) / bh;
+    if ((long long)p->N * tiles_w * tiles_h * tg->ngb > INT_MAX) return false;
+    kp->tile_w = bw;
+    kp->tile_h = bh;
+    kp->tiles_w = (int)tiles_w;
+    kp->tiles_h = (int)tiles_h;
+    return dcn::encode_input_map(*kp, *tg, p->dtype, in, map);
+  }
+  return false;
+}
+
 // Channels per thread of the backward: a power of two dividing gc, at most 4
 // (or DCN_BWD_CPT), with gc/c a power of two no larger than 32 so that a
 // unit's threads are adjacent lanes of one warp; 0 selects the kernel that
@@ -403,8 +476,14 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
                        (row_stride * es) % 32 == 0 && env_int("DCN_FWD_ROW64", 1);
   }
   const int cpt = pick_fwd_cpt(p, g, input, output);
-  if (cpt < 0) plan_fwd_tiles(p, g, -cpt, &kp);
+  alignas(64) unsigned char map[128];
+  dcn::TileGeom tg;
+  const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map);
+  if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
+  if (tile)
+    return cuda_status(dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset, mask,
+                                            output, static_cast<cudaStream_t>(stream)));
   return cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
                                      static_cast<cudaStream_t>(stream)));
 }
@@ -532,5 +611,10 @@ const char* dcn_status_str(int status) {
 }
 
 int dcn_version(void) { return 100; }
+
+int dcn_wait_timeouts(unsigned long long* count) {
+  if (!count) return DCN_ERR_NULL;
+  return cuda_status(dcn::read_wait_timeouts(count));
+}
 
 }  // extern "C"

@@ -65,6 +65,21 @@ struct WinGeom {
   int org_y, org_x;
 };
 
+// Geometry of the TMA-staged forward (fwd_tile_kernel): a block covers the
+// output tile of kp (tile_w x tile_h pixels) for GB consecutive groups, and
+// loads the input window of WH x WW pixels x GB*gc channels at
+// (ho0*stride_h + org_y, wo0*stride_w + org_x) into shared memory with one
+// tensor copy; ngb = G / GB blocks cover the groups of a tile.
+// swz != 0: a window pixel is exactly 128 bytes and the copy applies the
+// 128-byte swizzle (16-byte chunk j of pixel q at chunk j ^ (q & 7)).
+struct TileGeom {
+  int GB, ngb;
+  int WH, WW;
+  int org_y, org_x;
+  unsigned win_bytes;
+  int swz;
+};
+
 // Shared memory of bwd_window_kernel: TH*TW*P sample entries in cell order
 // (16 B each), the tile's grad_out (gc*es bytes per output pixel), and
 // per-cell counts, list heads and cursors ((WH-1)*(WW-1) cells).
@@ -85,6 +100,58 @@ __host__ __device__ inline size_t split_smem_bytes(const WinGeom& wg, int P, int
   auto up16 = [](size_t b) { return (b + 15) / 16 * 16; };
   return up16(nsamp * (es == 2 ? 8 : 16)) + up16(nsamp * 2) + nunit * gc * es +
          (2 * ncell + 1 + 32) * sizeof(int);
+}
+
+// ---- asynchronous tensor copies (TMA) and their barrier --------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// one arrival that also announces the bytes the copy will deliver
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for phase `parity` of the barrier at most `limit` polls (each poll
+// itself blocks for a hardware-defined time); false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int limit) {
+  for (int i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// A 4-D tiled copy global -> shared, completing on the barrier; coordinates
+// innermost first, out-of-range elements read as zero.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // ---- storage dtype traits ---------------------------------------------------

@@ -1,0 +1,350 @@
+// dcn_fwd_tma.cu -- the forward with the input window staged in shared memory.
+//
+// The FlashInternImage page, section 2.2, describes the fused kernel as
+// block-scheduled with the input tile staged in shared memory.  Here a block
+// covers an 8x8-style tile of output pixels for GB groups, and one tensor copy
+// (TMA, cp.async.bulk.tensor) brings the input window those pixels can sample
+// -- the footprint of their taps plus a halo of R pixels for the offsets --
+// into shared memory while the threads load their offsets and masks.  Pixels
+// of the window outside the image arrive as zeros, which is exactly the zero
+// padding of the op, so a sample whose bilinear cell lies in the window reads
+// its four corners from shared memory with no bounds logic.  A sample whose
+// cell leaves the window (large offsets, rare) reads its corners from global
+// memory as the wide forward does.  Same arithmetic as the wide forward
+// (dcn_fwd.cu): binary32 locations, mixed-precision FMAs into float32.
+//
+// The block's wait for the copy is bounded.  If it runs out, the block counts
+// it (dcn_wait_timeouts) and computes every sample from global memory, which
+// gives the same result; before it exits it waits once more, bounded, so that
+// no copy into its shared memory is left in flight.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <mutex>
+
+#include "dcn_common.cuh"
+#include "dcn_kernels.h"
+
+namespace dcn {
+
+__device__ unsigned long long g_wait_timeouts = 0;
+
+// Polls of the barrier before a block gives up on its copy (each poll blocks
+// for a hardware-defined time, so this is seconds, far beyond any copy).
+constexpr int kWaitPolls = 1 << 22;
+
+// v (NW words, NW/4 chunks of 16 bytes) rotated so that chunk j holds the
+// former chunk (j + rot) mod NC; selects only, registers stay registers.
+template <int NW>
+__device__ __forceinline__ void rotate_chunks(uint32_t (&v)[NW], int rot) {
+  constexpr int NC = NW / 4;
+  if constexpr (NC > 1) {
+    uint32_t o[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) o[i] = v[i];
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t x = o[4 * j + e];
+#pragma unroll
+        for (int r = 1; r < NC; ++r) x = rot == r ? o[4 * ((j + r) % NC) + e] : x;
+        v[4 * j + e] = x;
+      }
+  }
+}
+
+// The inverse for the accumulator (CPT floats = NC chunks of 4 floats when a
+// chunk holds 4 channels... of the storage type): channel chunk c is in slot
+// (c - rot) mod NC.  Chunks here are 16 bytes of storage, i.e. 16/sizeof(T)
+// channels.
+template <int CPT, typename T>
+__device__ __forceinline__ void unrotate_acc_t(float (&acc)[CPT], int rot) {
+  constexpr int PER = 16 / (int)sizeof(T);  // channels per 16-byte chunk
+  constexpr int NC = CPT / PER;
+  if constexpr (NC > 1) {
+    float o[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) o[i] = acc[i];
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        float x = o[PER * c + e];
+#pragma unroll
+        for (int r = 1; r < NC; ++r) x = rot == r ? o[PER * ((c - r + NC) % NC) + e] : x;
+        acc[PER * c + e] = x;
+      }
+  }
+}
+
+template <typename T, int CPT, int KP>
+__global__ void __launch_bounds__(256)
+fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, const TileGeom tg,
+                const T* __restrict__ input, const T* __restrict__ offset,
+                const T* __restrict__ mask, T* __restrict__ output) {
+  constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words per corner slice
+  constexpr int NC = NW / 4;                    // 16-byte chunks per corner slice
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + tg.win_bytes);
+  const int chunks = kp.gc / CPT;
+
+  // block -> (image, tile, group block), the group block fastest: the blocks
+  // of one tile copy neighbouring channels of the same window pixels
+  const int gb = blockIdx.x % tg.ngb;
+  const int rest = blockIdx.x / tg.ngb;
+  const int tiles = kp.tiles_w * kp.tiles_h;
+  const int t = rest % tiles, n = rest / tiles;
+  const int ty = t / kp.tiles_w;
+  const int ho0 = ty * kp.tile_h, wo0 = (t - ty * kp.tiles_w) * kp.tile_w;
+  const int wy0 = ho0 * kp.stride_h + tg.org_y, wx0 = wo0 * kp.stride_w + tg.org_x;
+
+  if (threadIdx.x == 0) mbar_init(bar, 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar, tg.win_bytes);
+    tma_load_4d(smem, &tmap, bar, gb * tg.GB * kp.gc, wx0, wy0, n);
+  }
+
+  // thread -> (pixel of the tile, group of the block, channel slice)
+  const int per_px = tg.GB * chunks;
+  const int lp = threadIdx.x / per_px, r = threadIdx.x - lp * per_px;
+  const int gl = r / chunks, slice = r - gl * chunks;
+  const int g = gb * tg.GB + gl, c0 = slice * CPT;
+  const int ho = ho0 + lp / kp.tile_w, wo = wo0 + lp % kp.tile_w;
+  const bool active = lp < kp.tile_w * kp.tile_h && ho < kp.Ho && wo < kp.Wo;
+  const uint32_t unit = active ? ((n * (uint32_t)kp.Ho + ho) * kp.Wo + wo) * kp.G + g : 0;
+
+  const int P = KP > 0 ? KP : kp.P;
+  const T* mrow = mask + (size_t)unit * kp.os_mask;
+  const T* orow = offset + (size_t)unit * kp.os_off;
+  const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
+  const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
+  const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
+  const float ref_y = (float)(ho * kp.stride_h - kp.pad_h + kp.cen_h);
+  const float scale = kp.offset_scale;
+
+  UnitRows<T, KP> rows;
+  bool vec = false;
+  constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
+  if constexpr (kVecRows)
+    vec = active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
+
+  float mx = 0.f, inv = 1.f;
+  if (kp.softmax && active) {
+    mx = -INFINITY;
+    if (vec) {
+#pragma unroll
+      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) mx = fmaxf(mx, rows.msk(p));
+      float s = 0.f;
+#pragma unroll
+      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) s += expf(rows.msk(p) - mx);
+      inv = 1.f / s;
+    } else {
+      for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
+      float s = 0.f;
+      for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
+      inv = 1.f / s;
+    }
+  }
+
+  // the swizzled layout is defined on 1024-byte aligned shared memory; a
+  // window that is not (never expected) reads everything from global memory
+  const bool ready = mbar_wait_bounded(bar, 0, kWaitPolls) &&
+                     !(tg.swz && (smem_addr(smem) & 1023u));
+  if (!ready && active && r == 0 && lp == 0) atomicAdd(&g_wait_timeouts, 1ull);
+
+  if (active) {
+    float acc[CPT];
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) acc[i] = 0.f;
+    // this thread's slice inside a window pixel, and the pixel's size
+    const uint32_t rb = (uint32_t)(tg.GB * kp.gc) * (uint32_t)sizeof(T);
+    const uint32_t chunk0 = (uint32_t)(gl * kp.gc + c0) * (uint32_t)sizeof(T) / 16u;
+    // A 16-byte shared load is served eight lanes at a time: the lanes of two
+    // (or four) tile pixels.  Their window pixels are unrelated, so reading
+    // the slices' chunks in the same order would hit the same banks; each
+    // tile pixel slot starts its chunks at its own rotation instead, and the
+    // accumulator is rotated back before the store.
+    const int rot = NC > 1 ? lp & (NC - 1) : 0;
+    const uint32_t sbase = smem_addr(smem);
+    const int WWm = tg.WW - 1, WHm = tg.WH - 1;
+
+#pragma unroll(KP > 0 ? KP : 1)
+    for (int p = 0; p < P; ++p) {
+      float m;
+      float2 d;
+      if (KP > 0 && vec) {
+        m = rows.msk(KP > 0 ? p : 0);
+        d = rows.off(KP > 0 ? p : 0);
+      } else {
+        m = ld_once_1(mrow + p);
+        d = ld_once_2(orow + 2 * p);
+      }
+      if (kp.softmax) m = expf(m - mx) * inv;
+      const float x = location(d.x, kp.tap_x[p], scale, ref_x);
+      const float y = location(d.y, kp.tap_y[p], scale, ref_y);
+      if (!in_box(x, y, kp.W, kp.H)) continue;  // also NaN / inf
+      const float xf = floorf(x), yf = floorf(y);
+      const int x0 = (int)xf, y0 = (int)yf;
+      const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
+      const int cx = x0 - wx0, cy = y0 - wy0;
+      if (ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm) {
+        // the cell is in the window: corners from shared memory, zeros
+        // standing for pixels outside the image
+        const uint32_t a00 = sbase + (uint32_t)(cy * tg.WW + cx) * rb;
+        const uint32_t at[4] = {a00, a00 + rb, a00 + (uint32_t)tg.WW * rb,
+                                a00 + (uint32_t)tg.WW * rb + rb};
+        const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          // with the 128-byte swizzle, 16-byte chunk j of window pixel q sits
+          // at chunk position j ^ (q & 7) of the pixel's 128 bytes
+          const uint32_t sw =
+              tg.swz ? (uint32_t)(((cy + (k >> 1)) * tg.WW + cx + (k & 1)) & 7) : 0u;
+          uint32_t v[NW];
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            // accumulator chunk j takes the slice's chunk (j + rot) mod NC
+            const uint32_t cj = chunk0 + (uint32_t)((j + rot) & (NC - 1));
+            const uint4 c = lds128(at[k] + 16u * (cj ^ sw));
+            v[4 * j] = c.x;
+            v[4 * j + 1] = c.y;
+            v[4 * j + 2] = c.z;
+            v[4 * j + 3] = c.w;
+          }
+          fma_words<T, NW>(acc, v, Fma<T>::weight(w[k]));
+        }
+      } else {
+        // far sample: clamped corners from global memory, weight 0 outside
+        const float wy0v = (uint32_t)y0 < H ? gy * m : 0.f;
+        const float wy1v = (uint32_t)(y0 + 1) < H ? fy * m : 0.f;
+        const float wx0v = (uint32_t)x0 < W ? gx : 0.f;
+        const float wx1v = (uint32_t)(x0 + 1) < W ? fx : 0.f;
+        const uint32_t xa = min((uint32_t)x0, W - 1), xb = min((uint32_t)(x0 + 1), W - 1);
+        const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
+        const uint32_t ra = ya * WC, rbb = yb * WC, ca = xa * C, cb = xb * C;
+        uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
+        ldg_words<NW>(img + (ra + ca), v00);
+        ldg_words<NW>(img + (ra + cb), v01);
+        ldg_words<NW>(img + (rbb + ca), v10);
+        ldg_words<NW>(img + (rbb + cb), v11);
+        rotate_chunks<NW>(v00, rot);
+        rotate_chunks<NW>(v01, rot);
+        rotate_chunks<NW>(v10, rot);
+        rotate_chunks<NW>(v11, rot);
+        fma_words<T, NW>(acc, v00, Fma<T>::weight(wy0v * wx0v));
+        fma_words<T, NW>(acc, v01, Fma<T>::weight(wy0v * wx1v));
+        fma_words<T, NW>(acc, v10, Fma<T>::weight(wy1v * wx0v));
+        fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1v * wx1v));
+      }
+    }
+    unrotate_acc_t<CPT, T>(acc, rot);
+    Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
+  }
+  // a block whose wait ran out leaves no copy in flight into its memory
+  if (!ready) mbar_wait_bounded(bar, 0, kWaitPolls);
+}
+
+// ---- host side ------------------------------------------------------------------
+
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library links the runtime only).
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const void* input,
+                      void* map_out) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  CUtensorMapDataType dt;
+  size_t es;
+  switch (dtype) {
+    case DCN_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; es = 4; break;
+    case DCN_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; es = 2; break;
+    case DCN_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; es = 2; break;
+    default: return false;
+  }
+  const cuuint64_t dims[4] = {(cuuint64_t)kp.C, (cuuint64_t)kp.W, (cuuint64_t)kp.H,
+                              (cuuint64_t)kp.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)kp.C * es, (cuuint64_t)kp.W * kp.C * es,
+                                 (cuuint64_t)kp.H * kp.W * kp.C * es};
+  const cuuint32_t box[4] = {(cuuint32_t)(tg.GB * kp.gc), (cuuint32_t)tg.WW,
+                             (cuuint32_t)tg.WH, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUtensorMap* m = static_cast<CUtensorMap*>(map_out);
+  return enc(m, dt, 4, const_cast<void*>(input), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             tg.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int CPT>
+static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, const TileGeom& tg,
+                                 const T* i_, const T* o_, const T* m_, T* y_, cudaStream_t s) {
+  constexpr int bytes = CPT * (int)sizeof(T);
+  if constexpr (bytes >= 16 && bytes <= 64) {
+    const size_t smem = tg.win_bytes + 16;  // the window, then the barrier
+    auto k9 = fwd_tile_kernel<T, CPT, 9>;
+    auto k8 = fwd_tile_kernel<T, CPT, 8>;
+    auto k0 = fwd_tile_kernel<T, CPT, 0>;
+    auto k = kp.P == 9 ? k9 : kp.P == 8 ? k8 : k0;
+    if (smem > 48 * 1024) {
+      cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    const long long grid = (long long)kp.N * kp.tiles_w * kp.tiles_h * tg.ngb;
+    if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
+    k<<<(unsigned)grid, 256, smem, s>>>(map, kp, tg, i_, o_, m_, y_);
+    return cudaGetLastError();
+  } else {
+    return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_tile_d(const CUtensorMap& map, const KParams& kp, const TileGeom& tg,
+                                 int cpt, const void* in, const void* off, const void* msk,
+                                 void* out, cudaStream_t s) {
+  const T* i_ = static_cast<const T*>(in);
+  const T* o_ = static_cast<const T*>(off);
+  const T* m_ = static_cast<const T*>(msk);
+  T* y_ = static_cast<T*>(out);
+  switch (cpt) {
+    case 4: return launch_tile_t<T, 4>(map, kp, tg, i_, o_, m_, y_, s);
+    case 8: return launch_tile_t<T, 8>(map, kp, tg, i_, o_, m_, y_, s);
+    case 16: return launch_tile_t<T, 16>(map, kp, tg, i_, o_, m_, y_, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& tg, int dtype,
+                            int cpt, const void* in, const void* off, const void* msk, void* out,
+                            cudaStream_t s) {
+  const CUtensorMap& m = *static_cast<const CUtensorMap*>(map);
+  switch (dtype) {
+    case DCN_F32: return launch_tile_d<float>(m, kp, tg, cpt, in, off, msk, out, s);
+    case DCN_F16: return launch_tile_d<__half>(m, kp, tg, cpt, in, off, msk, out, s);
+    case DCN_BF16: return launch_tile_d<__nv_bfloat16>(m, kp, tg, cpt, in, off, msk, out, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t read_wait_timeouts(unsigned long long* count) {
+  return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned long long));
+}
+
+}  // namespace dcn

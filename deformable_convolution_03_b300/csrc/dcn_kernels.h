@@ -46,4 +46,17 @@ cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, in
                              const void* msk, float* gin_acc, void* gin, void* goff, void* gmask,
                              cudaStream_t s);
 
+// The TMA-staged forward (dcn_fwd_tma.cu).  encode_input_map fills the
+// 128-byte tensor map of the input (dims C, W, H, N; box GB*gc x WW x WH x 1;
+// out-of-range elements read as zero) and returns false when the driver
+// rejects it; launch_fwd_tile runs fwd_tile_kernel with cpt as the wide
+// forward's (16 to 64 bytes per slice) over the tiles of kp.
+bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const void* input,
+                      void* map_out);
+cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& tg, int dtype,
+                            int cpt, const void* in, const void* off, const void* msk, void* out,
+                            cudaStream_t s);
+// Blocks whose bounded wait for a tensor copy ran out, since load.
+cudaError_t read_wait_timeouts(unsigned long long* count);
+
 }  // namespace dcn

@@ -181,6 +181,15 @@ int dcn_core_bwd_noalloc(const dcn_params_t* p, const void* grad_out, const void
                          const void* offset, const void* mask, void* grad_input,
                          void* grad_offset, void* grad_mask, void* stream);
 
+/* Diagnostics of the asynchronous tensor copies some kernels use: the number
+ * of thread blocks, since the library was loaded, whose bounded wait for such a
+ * copy ran out on the current device.  Such a block computed its results from
+ * global memory instead, so results stay correct; a non-zero count means a
+ * copy took seconds, i.e. something is wrong with the device.  Reads a device
+ * counter synchronously (the current device).  DCN_ERR_NULL for a NULL
+ * count, DCN_ERR_CUDA if the read fails. */
+int dcn_wait_timeouts(unsigned long long* count);
+
 /* A static, human-readable name for a dcn_status_t. */
 const char* dcn_status_str(int status);
 

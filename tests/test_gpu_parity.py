@@ -111,8 +111,35 @@ def test_every_general_kernel_instance(dt, cap, monkeypatch):
 def test_wide_forward_instances(dt, gc, sm, rc, tile, monkeypatch):
     # slices of 4, 8 and 16 channels, 9 points and the runtime point count,
     # blocks over 2-D pixel tiles and over consecutive items
+    monkeypatch.setenv("DCN_FWD_TMA", "0")
     monkeypatch.setenv("DCN_FWD_TILE", tile)
     w = small(f"wide_{dt}_{gc}", dt, gc=gc, G=3, softmax=sm, remove_center=rc, N=2, H=11, W=13)
+    check_fwd(w, make_inputs(w))
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("gc,G", [(8, 4), (16, 4), (16, 8), (32, 4), (48, 2)])
+@pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
+@pytest.mark.parametrize("halo", ["6", "2", "0"])
+def test_tma_forward_instances(dt, gc, G, sm, rc, halo, monkeypatch):
+    # the forward with its input window staged by a tensor copy: every slice
+    # width, one or several blocks per tile's groups (a pixel's channels over
+    # 128 bytes), the 9-point, 8-point and runtime instances; halos of 6, 2
+    # and 0 pixels send more and more samples through the far path
+    monkeypatch.setenv("DCN_FWD_HALO", halo)
+    w = small(f"tma_{dt}_{gc}_{G}", dt, gc=gc, G=G, softmax=sm, remove_center=rc, N=2, H=19,
+              W=21, offset_std=3.0)
+    check_fwd(w, make_inputs(w))
+
+
+@pytest.mark.parametrize("geom", ["s2d2", "k5", "k7rc", "k1"])
+def test_tma_forward_geometries(geom):
+    # windows for strided, dilated and larger kernels, and for 1x1
+    over = {"s2d2": dict(stride_h=2, stride_w=2, dilation_h=2, dilation_w=2),
+            "k5": dict(kernel_h=5, kernel_w=5, pad_h=2, pad_w=2, offset_scale=0.5),
+            "k7rc": dict(kernel_h=7, kernel_w=7, pad_h=3, pad_w=3, remove_center=1),
+            "k1": dict(kernel_h=1, kernel_w=1, pad_h=0, pad_w=0)}[geom]
+    w = small(f"tmag_{geom}", "bf16", gc=16, G=4, N=2, H=23, W=26, **over)
     check_fwd(w, make_inputs(w))
 
 
@@ -327,3 +354,8 @@ def test_more_than_2_31_input_elements():
                                                                                device="cuda")
         assert torch.equal(out[n, y, xx], want), (n, y, xx)
     assert torch.equal(out[N - 1, ho - 3, wo - 3], x[N - 1, ho - 4, wo - 1])
+
+
+def test_no_tensor_copy_wait_ran_out():
+    # every tensor copy the tests above waited for arrived in time
+    assert B.dcn_wait_timeouts() == 0
