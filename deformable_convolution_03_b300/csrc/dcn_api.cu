@@ -253,7 +253,6 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
     tg->org_y = -p->pad_h + ch + tmin_y - R;
     tg->org_x = -p->pad_w + cw + tmin_x - R;
     tg->win_bytes = (unsigned)(WH * WW * rb);
-    tg->swz = rb == 128 && env_int("DCN_FWD_SWIZZLE", 0);
     const long long tiles_w = (g.Wo + bw - 1) / bw, tiles_h = (g.Ho + bh - 1) / bh;
     if ((long long)p->N * tiles_w * tiles_h * tg->ngb > INT_MAX) return false;
     kp->tile_w = bw;

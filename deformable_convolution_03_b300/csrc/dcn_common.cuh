@@ -70,14 +70,11 @@ struct WinGeom {
 // loads the input window of WH x WW pixels x GB*gc channels at
 // (ho0*stride_h + org_y, wo0*stride_w + org_x) into shared memory with one
 // tensor copy; ngb = G / GB blocks cover the groups of a tile.
-// swz != 0: a window pixel is exactly 128 bytes and the copy applies the
-// 128-byte swizzle (16-byte chunk j of pixel q at chunk j ^ (q & 7)).
 struct TileGeom {
   int GB, ngb;
   int WH, WW;
   int org_y, org_x;
   unsigned win_bytes;
-  int swz;
 };
 
 // Shared memory of bwd_window_kernel: TH*TW*P sample entries in cell order

@@ -86,7 +86,7 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
                 const T* __restrict__ mask, T* __restrict__ output) {
   constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words per corner slice
   constexpr int NC = NW / 4;                    // 16-byte chunks per corner slice
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + tg.win_bytes);
   const int chunks = kp.gc / CPT;
 
@@ -149,10 +149,7 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
     }
   }
 
-  // the swizzled layout is defined on 1024-byte aligned shared memory; a
-  // window that is not (never expected) reads everything from global memory
-  const bool ready = mbar_wait_bounded(bar, 0, kWaitPolls) &&
-                     !(tg.swz && (smem_addr(smem) & 1023u));
+  const bool ready = mbar_wait_bounded(bar, 0, kWaitPolls);
   if (!ready && active && r == 0 && lp == 0) atomicAdd(&g_wait_timeouts, 1ull);
 
   if (active) {
@@ -168,6 +165,9 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
     // tile pixel slot starts its chunks at its own rotation instead, and the
     // accumulator is rotated back before the store.
     const int rot = NC > 1 ? lp & (NC - 1) : 0;
+    uint32_t coff[NC];  // byte offset in a window pixel of accumulator chunk j
+#pragma unroll
+    for (int j = 0; j < NC; ++j) coff[j] = 16u * (chunk0 + (uint32_t)((j + rot) & (NC - 1)));
     const uint32_t sbase = smem_addr(smem);
     const int WWm = tg.WW - 1, WHm = tg.WH - 1;
 
@@ -199,16 +199,11 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
         const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          // with the 128-byte swizzle, 16-byte chunk j of window pixel q sits
-          // at chunk position j ^ (q & 7) of the pixel's 128 bytes
-          const uint32_t sw =
-              tg.swz ? (uint32_t)(((cy + (k >> 1)) * tg.WW + cx + (k & 1)) & 7) : 0u;
           uint32_t v[NW];
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             // accumulator chunk j takes the slice's chunk (j + rot) mod NC
-            const uint32_t cj = chunk0 + (uint32_t)((j + rot) & (NC - 1));
-            const uint4 c = lds128(at[k] + 16u * (cj ^ sw));
+            const uint4 c = lds128(at[k] + coff[j]);
             v[4 * j] = c.x;
             v[4 * j + 1] = c.y;
             v[4 * j + 2] = c.z;
@@ -286,8 +281,7 @@ bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const vo
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUtensorMap* m = static_cast<CUtensorMap*>(map_out);
   return enc(m, dt, 4, const_cast<void*>(input), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE,
-             tg.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
