@@ -203,7 +203,7 @@ void plan_fwd_tiles(const dcn_params_t* p, const Geometry& g, int cpt, dcn::KPar
 constexpr size_t kTileSmem = 64 * 1024;
 
 bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void* in,
-                   dcn::KParams* kp, dcn::TileGeom* tg, void* map) {
+                   dcn::KParams* kp, dcn::TileGeom* tg, void* map, size_t budget = kTileSmem) {
   if (!env_int("DCN_FWD_TMA", 1)) return false;
   const int es = elem_size(p->dtype);
   const long long C = (long long)p->G * p->gc;
@@ -245,7 +245,7 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
   for (int R = env_int("DCN_FWD_HALO", 6); R >= 0; --R) {
     const long long WH = (long long)(bh - 1) * p->stride_h + (tmax_y - tmin_y) + 2 + 2 * R;
     const long long WW = (long long)(bw - 1) * p->stride_w + (tmax_x - tmin_x) + 2 + 2 * R;
-    if (WH > 256 || WW > 256 || (size_t)(WH * WW) * rb > kTileSmem) continue;
+    if (WH > 256 || WW > 256 || (size_t)(WH * WW) * rb > budget) continue;
     tg->GB = GB;
     tg->ngb = p->G / GB;
     tg->WH = (int)WH;
@@ -367,7 +367,9 @@ constexpr size_t kSplitSmem = 56 * 1024;
 constexpr size_t kStageSmem = 32 * 1024;
 
 int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const void* gout,
-               const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb) {
+               const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb,
+               dcn::TileGeom* tg, void* map, bool* tma) {
+  *tma = false;
   const int mode = env_int("DCN_BWD_SPLIT", 2);
   if (mode == 0 || (mode != 1 && p->dtype == DCN_F32)) return 0;
   const int es = elem_size(p->dtype);
@@ -411,7 +413,17 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     }
   }
   if (best < 0 || (long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
-  plan_fwd_tiles(p, g, cpt, kp);
+  // the sample blocks read their corners through L1 over the wide forward's
+  // tiles.  DCN_BWD_TMA=1 stages their input windows by a tensor copy instead
+  // (the forward's TMA plan, windows within DCN_BWD_TMA_KB KB): measured
+  // slower inside the fused launch (FlashInternImage-T stage 1: 315-326 us
+  // against 272 us), whose input blocks then get less L1.
+  const bool fused = env_int("DCN_BWD_FUSE", 1) != 0;
+  const size_t tma_budget = (size_t)env_int("DCN_BWD_TMA_KB", 40) * 1024;
+  if (fused && env_int("DCN_BWD_TMA", 0) && plan_fwd_tile(p, g, cpt, in, kp, tg, map, tma_budget))
+    *tma = true;
+  else
+    plan_fwd_tiles(p, g, cpt, kp);
   // grad_offset / grad_mask rows staged in shared memory
   const int ub = 256 / chunks;
   if (kp->merged) {
@@ -422,6 +434,9 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     *lb = g.P;
   }
   if (!env_int("DCN_BWD_STAGE", 1) || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
+  // staged rows are copied out per tile row, which needs every group of a
+  // pixel in the block
+  if (*tma && tg->GB != p->G) *la = *lb = 0;
   return cpt;
 }
 
@@ -548,7 +563,10 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
   }
   dcn::WinGeom wg;
   int la = 0, lb = 0;
-  const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb);
+  dcn::TileGeom tg;
+  alignas(64) unsigned char map[128];
+  bool tma = false;
+  const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb, &tg, map, &tma);
   const int wcpt = scpt ? 0 : plan_window(p, g, input, grad_out, acc, &wg);
   const int cpt = scpt || wcpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
   if (fault_injected()) return DCN_ERR_CUDA;
@@ -560,7 +578,7 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
   if (scpt)
     return cuda_status(dcn::launch_bwd_split(kp, wg, p->dtype, scpt, la, lb, grad_out, input,
                                              offset, mask, acc, grad_input, grad_offset,
-                                             grad_mask, s));
+                                             grad_mask, tma ? map : nullptr, &tg, s));
   if (wcpt)
     return cuda_status(dcn::launch_bwd_window(kp, wg, p->dtype, wcpt, grad_out, input, offset,
                                               mask, acc, grad_input, grad_offset, grad_mask, s));
@@ -613,7 +631,11 @@ int dcn_version(void) { return 100; }
 
 int dcn_wait_timeouts(unsigned long long* count) {
   if (!count) return DCN_ERR_NULL;
-  return cuda_status(dcn::read_wait_timeouts(count));
+  unsigned long long a = 0, b = 0;
+  if (dcn::read_wait_timeouts(&a) != cudaSuccess || dcn::read_split_wait_timeouts(&b) != cudaSuccess)
+    return DCN_ERR_CUDA;
+  *count = a + b;
+  return DCN_OK;
 }
 
 }  // extern "C"

@@ -399,6 +399,27 @@ struct UnitRows {
   }
 };
 
+// v (NW words, NW/4 chunks of 16 bytes) rotated so that chunk j holds the
+// former chunk (j + rot) mod NC; selects only, registers stay registers.
+template <int NW>
+__device__ __forceinline__ void rotate_chunks(uint32_t (&v)[NW], int rot) {
+  constexpr int NC = NW / 4;
+  if constexpr (NC > 1) {
+    uint32_t o[NW];
+#pragma unroll
+    for (int i = 0; i < NW; ++i) o[i] = v[i];
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        uint32_t x = o[4 * j + e];
+#pragma unroll
+        for (int r = 1; r < NC; ++r) x = rot == r ? o[4 * ((j + r) % NC) + e] : x;
+        v[4 * j + e] = x;
+      }
+  }
+}
+
 // acc[0..2*NW) += weight * (the 16-bit or 32-bit elements packed in w), one
 // product per element, accumulated in float32.  16-bit storage: the weight is
 // rounded to the storage type once and each product is exact in float32

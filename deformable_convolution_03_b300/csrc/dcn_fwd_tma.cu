@@ -34,27 +34,6 @@ __device__ unsigned long long g_wait_timeouts = 0;
 // for a hardware-defined time, so this is seconds, far beyond any copy).
 constexpr int kWaitPolls = 1 << 22;
 
-// v (NW words, NW/4 chunks of 16 bytes) rotated so that chunk j holds the
-// former chunk (j + rot) mod NC; selects only, registers stay registers.
-template <int NW>
-__device__ __forceinline__ void rotate_chunks(uint32_t (&v)[NW], int rot) {
-  constexpr int NC = NW / 4;
-  if constexpr (NC > 1) {
-    uint32_t o[NW];
-#pragma unroll
-    for (int i = 0; i < NW; ++i) o[i] = v[i];
-#pragma unroll
-    for (int j = 0; j < NC; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        uint32_t x = o[4 * j + e];
-#pragma unroll
-        for (int r = 1; r < NC; ++r) x = rot == r ? o[4 * ((j + r) % NC) + e] : x;
-        v[4 * j + e] = x;
-      }
-  }
-}
-
 // The inverse for the accumulator (CPT floats = NC chunks of 4 floats when a
 // chunk holds 4 channels... of the storage type): channel chunk c is in slot
 // (c - rot) mod NC.  Chunks here are 16 bytes of storage, i.e. 16/sizeof(T)

@@ -41,10 +41,14 @@ cudaError_t launch_bwd_window(const KParams& kp, const WinGeom& wg, int dtype, i
 // staged offset and mask rows (0: written straight to memory).  gin_acc
 // (float32) must be cleared by the caller; when it is not gin, it is rounded
 // into gin at the end.
+// map / tg: when map is not NULL, the sample blocks of the fused launch
+// stage their input windows with that tensor map over the tiles of kp and tg
+// (see encode_input_map); otherwise they read through L1 over kp's tiles.
 cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, int cpt, int la,
                              int lb, const void* gout, const void* in, const void* off,
                              const void* msk, float* gin_acc, void* gin, void* goff, void* gmask,
-                             cudaStream_t s);
+                             const void* map, const TileGeom* tg, cudaStream_t s);
+cudaError_t read_split_wait_timeouts(unsigned long long* count);
 
 // The TMA-staged forward (dcn_fwd_tma.cu).  encode_input_map fills the
 // 128-byte tensor map of the input (dims C, W, H, N; box GB*gc x WW x WH x 1;

@@ -31,6 +31,7 @@ CASES = [
 BWD = {
     "default": {},
     "split": {"DCN_BWD_SPLIT": "1"},
+    "split_tma": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1"},
     "single_pass": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "0"},
 }
 

@@ -171,6 +171,10 @@ BWD_MODES = {
     "split_direct": {"DCN_BWD_SPLIT": "1", "DCN_BWD_STAGE": "0", "DCN_FWD_TILE": "0"},
     # the two split kernels as separate launches instead of one
     "split_unfused": {"DCN_BWD_SPLIT": "1", "DCN_BWD_FUSE": "0"},
+    # the fused launch with the sample blocks' input windows staged by a
+    # tensor copy, with a small window (many far samples)
+    "split_tma": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1"},
+    "split_tma_small": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1", "DCN_BWD_TMA_KB": "8"},
     # the fused windowed kernel, with its default halo and with one pixel
     "window": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1"},
     "window_halo1": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1", "DCN_BWD_HALO": "1"},
