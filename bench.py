@@ -52,12 +52,12 @@ FALLBACK_HBM_GBS = 6400.0
 # workload, with the sha1 of the kernel source it was taken on: a changed
 # source voids the figure.
 TRAFFIC = {
-    # profiles/launches_t_stage1_f16.md: fwd_wide_kernel, per launch
-    "fwd@t_stage1_f16": {"bytes": 69_081_767 + 1_295_983, "sha": "8557bc1c4bfa"},
+    # profiles/launches_t_stage1_f16.md: fwd_tile_kernel, per launch
+    "fwd@t_stage1_f16": {"bytes": 69_102_581 + 774_689, "sha": "980bf0c14887"},
     # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
     # call (the accumulator's memset is not a kernel and is not counted)
-    "bwd@t_stage1_f16": {"bytes": 169_838_959 + 44_507_136 + 51_389_184 + 112_506,
-                         "sha": "3dcfb874fec6"},
+    "bwd@t_stage1_f16": {"bytes": 169_852_694 + 44_502_840 + 51_389_473 + 104_225,
+                         "sha": "0f47884a8933"},
 }
 
 
@@ -479,8 +479,8 @@ def main():
                 "ms": round(bwd_ms, 5), "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "fwd": {"bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(fwd_gbs / peak, 4),
-                "traffic": traffic_for(f"fwd@{w.name}", ("dcn_fwd.cu",)) if args.layout == "separate" else None,
-                "phase": "dcn_core_fwd: fwd_wide_kernel", "ms": round(fwd_ms, 5),
+                "traffic": traffic_for(f"fwd@{w.name}", ("dcn_fwd_tma.cu",)) if args.layout == "separate" else None,
+                "phase": "dcn_core_fwd: fwd_tile_kernel (TMA-staged)", "ms": round(fwd_ms, 5),
                 "peak_source": f"{peak_kind} HBM copy bandwidth"},
     }
 

@@ -904,12 +904,12 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
 // and shared-memory-bound input blocks side by side instead of one kind after
 // the other.  The two halves share no data: the sample half writes grad_offset
 // and grad_mask, the input half reduces into the cleared accumulator.
-// With tma != 0 the sample blocks stage their input window by a tensor copy
+// With kTma the sample blocks stage their input window by a tensor copy
 // (sample_block_tma over the tiles of kp and tg); otherwise they read their
 // corners through L1 (sample_block).
-template <typename T, int CPT, int NW, int KP>
+template <typename T, int CPT, int NW, int KP, bool kTma>
 __global__ void __launch_bounds__(256, 3)
-bwd_both_kernel(const __grid_constant__ CUtensorMap tmap, const TileGeom tg, int tma,
+bwd_both_kernel(const __grid_constant__ CUtensorMap tmap, const TileGeom tg,
                 const KParams kp, const WinGeom wg, const T* __restrict__ gout,
                 const T* __restrict__ input, const T* __restrict__ offset,
                 const T* __restrict__ mask, T* __restrict__ goff, T* __restrict__ gmask, int la,
@@ -925,7 +925,7 @@ bwd_both_kernel(const __grid_constant__ CUtensorMap tmap, const TileGeom tg, int
     id = b - m;
   }
   if (sample) {
-    if (tma)
+    if constexpr (kTma)
       sample_block_tma<T, CPT, KP>(&tmap, kp, tg, gout, input, offset, mask, goff, gmask, la,
                                    lb, id);
     else
@@ -1005,10 +1005,12 @@ static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* 
                     (la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0);
   const size_t sb = split_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
   const size_t smem = sa > sb ? sa : sb;
-  auto k9 = bwd_both_kernel<T, CPT, NW, 9>;
-  auto k8 = bwd_both_kernel<T, CPT, NW, 8>;
-  auto k0 = bwd_both_kernel<T, CPT, NW, 0>;
-  auto k = kp.P == 9 ? k9 : kp.P == 8 ? k8 : k0;
+  auto k = map ? (kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9, true>
+                            : kp.P == 8 ? bwd_both_kernel<T, CPT, NW, 8, true>
+                                        : bwd_both_kernel<T, CPT, NW, 0, true>)
+               : (kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9, false>
+                            : kp.P == 8 ? bwd_both_kernel<T, CPT, NW, 8, false>
+                                        : bwd_both_kernel<T, CPT, NW, 0, false>);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1017,8 +1019,8 @@ static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* 
   std::memset(&none, 0, sizeof none);
   const TileGeom tg0 = tg ? *tg : TileGeom{};
   k<<<(unsigned)(na + nb), block, smem, s>>>(
-      map ? *static_cast<const CUtensorMap*>(map) : none, tg0, map ? 1 : 0, kp, wg, go_, i_, o_,
-      m_, goff_, gm_, la, lb, acc, (unsigned)na, (unsigned)nb);
+      map ? *static_cast<const CUtensorMap*>(map) : none, tg0, kp, wg, go_, i_, o_, m_, goff_,
+      gm_, la, lb, acc, (unsigned)na, (unsigned)nb);
   return cudaGetLastError();
 }
 
