@@ -79,7 +79,7 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
                                              T* __restrict__ gmask, int la, int lb,
                                              const unsigned bid) {
   constexpr int NW = CPT * (int)sizeof(T) / 4;
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int chunks = kp.gc / CPT;
   const int P = KP > 0 ? KP : kp.P;
   uint32_t unit = 0, n;
@@ -566,7 +566,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
   // one row of its corners: (x0, x1) as 2 x 16 bits or 2 x float32
   using Wq = typename std::conditional<k16, uint2, float4>::type;
   using Wh = typename std::conditional<k16, uint32_t, float2>::type;
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int P = KP > 0 ? KP : kp.P;
   const int nunit = wg.TH * wg.TW;
   const int nsamp = nunit * P;
