@@ -32,7 +32,7 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
-           "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
+           "dcn_linear", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -98,6 +98,7 @@ def lib() -> ctypes.CDLL:
         L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t,
                                       vp]
         L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+        L.dcn_linear.argtypes = [ctypes.POINTER(dcn_linear_params_t), vp, vp, vp, vp, vp]
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -131,6 +132,34 @@ def dcn_status_str(status: int) -> str:
 
 def dcn_version() -> int:
     return int(lib().dcn_version())
+
+
+class dcn_linear_params_t(ctypes.Structure):
+    """Mirror of dcn_linear_params_t (include/dcn_core.h)."""
+    _fields_ = [("M", ctypes.c_longlong), ("K", ctypes.c_int), ("N", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+def dcn_linear(x, w, bias, y, stream=None) -> None:
+    """Raw entry point: y = x w^T + bias over the rows of x (all of one dtype)."""
+    M, K = int(x.shape[0]), int(x.shape[1])
+    p = dcn_linear_params_t(M, K, int(w.shape[0]), TORCH_TO_DCN[x.dtype])
+    _check(lib().dcn_linear(ctypes.byref(p), _ptr(x), _ptr(w), _ptr(bias), _ptr(y),
+                            _stream(stream)), "dcn_linear")
+
+
+def linear(x, w, bias=None):
+    """y = x w^T + bias on the GPU, x (..., K) channels-last, w (N, K)."""
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError("linear: contiguous CUDA tensors of one dtype expected")
+    K = x.shape[-1]
+    if w.dim() != 2 or w.shape[1] != K or (bias is not None and bias.shape != (w.shape[0],)):
+        raise ValueError(f"linear: shapes {tuple(x.shape)}, {tuple(w.shape)} do not match")
+    x2 = x.reshape(-1, K)
+    y = torch.empty(x2.shape[0], w.shape[0], dtype=x.dtype, device=x.device)
+    dcn_linear(x2, w, bias, y, torch.cuda.current_stream(x.device).cuda_stream)
+    return y.reshape(*x.shape[:-1], w.shape[0])
 
 
 def dcn_wait_timeouts() -> int:

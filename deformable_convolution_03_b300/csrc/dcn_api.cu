@@ -631,11 +631,31 @@ int dcn_version(void) { return 100; }
 
 int dcn_wait_timeouts(unsigned long long* count) {
   if (!count) return DCN_ERR_NULL;
-  unsigned long long a = 0, b = 0;
-  if (dcn::read_wait_timeouts(&a) != cudaSuccess || dcn::read_split_wait_timeouts(&b) != cudaSuccess)
+  unsigned long long a = 0, b = 0, c = 0;
+  if (dcn::read_wait_timeouts(&a) != cudaSuccess ||
+      dcn::read_split_wait_timeouts(&b) != cudaSuccess ||
+      dcn::read_linear_wait_timeouts(&c) != cudaSuccess)
     return DCN_ERR_CUDA;
-  *count = a + b;
+  *count = a + b + c;
   return DCN_OK;
+}
+
+int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const void* bias,
+               void* y, void* stream) {
+  if (!p) return DCN_ERR_NULL;
+  const int es = elem_size(p->dtype);
+  if (es == 0) return DCN_ERR_DTYPE;
+  if (p->M < 0 || p->K < 1 || p->N < 1) return DCN_ERR_SHAPE;
+  if (p->M > (1LL << 40) / p->K || p->M > (1LL << 40) / p->N) return DCN_ERR_UNSUPPORTED;
+  if (p->M == 0) return DCN_OK;
+  if (!x || !w || !y) return DCN_ERR_NULL;
+  if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || (bias && !aligned(bias, es)))
+    return DCN_ERR_ALIGN;
+  const bool tc = env_int("DCN_LINEAR_TC", 1) && dcn::linear_tc_ok(p->dtype, p->M, p->K, p->N,
+                                                                   x, w, y);
+  if (fault_injected()) return DCN_ERR_CUDA;
+  return cuda_status(dcn::launch_linear(p->dtype, p->M, p->K, p->N, x, w, bias, y, tc,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -181,6 +181,36 @@ int dcn_core_bwd_noalloc(const dcn_params_t* p, const void* grad_out, const void
                          const void* offset, const void* mask, void* grad_input,
                          void* grad_offset, void* grad_mask, void* stream);
 
+/* The linear projections around the core op: y = x W^T + b, over the rows of
+ * a channels-last tensor.  The DCN module feeds the core through such layers:
+ * DCNv3's input, offset, mask and output projections (page
+ * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
+ * items 1-6), and DCNv4's one merged offset/mask projection, whose output is
+ * the offset_mask tensor of dcn_core_fwd_om when its weight rows are laid out
+ * per group as 2P offsets, P mask values and zero padding (page
+ * "告别DCNv3的卡顿：实测DCNv4在A100上3倍提速，手把手教你集成到FlashInternImage",
+ * section 1).
+ *   x     (M, K)  row-major, read
+ *   w     (N, K)  row-major (a linear layer's weight), read
+ *   bias  (N)     or NULL, read
+ *   y     (M, N)  row-major, fully overwritten
+ * One dtype for all four.  Arithmetic: float32 accumulation, one rounding to
+ * the storage type.  For float16 / bfloat16 with K a multiple of 64 up to 256,
+ * N a multiple of 16 from 16 to 256 and x, w, y 16-byte aligned, the product
+ * runs on the tensor cores (tcgen05, operands staged by tensor copies);
+ * otherwise one CUDA thread per output element.  M == 0 launches nothing.
+ * DCN_ERR_NULL / DCN_ERR_SHAPE (M < 0, K < 1, N < 1) / DCN_ERR_DTYPE /
+ * DCN_ERR_ALIGN (a pointer not aligned to the element size) on bad
+ * arguments, before any CUDA call. */
+typedef struct {
+  long long M;  /* rows */
+  int K, N;     /* input and output features */
+  int dtype;    /* dcn_dtype_t of x, w, bias and y */
+} dcn_linear_params_t;
+
+int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const void* bias,
+               void* y, void* stream);
+
 /* Diagnostics of the asynchronous tensor copies some kernels use: the number
  * of thread blocks, since the library was loaded, whose bounded wait for such a
  * copy ran out on the current device.  Such a block computed its results from

@@ -181,3 +181,29 @@ def test_merged_layout_argument_checks(native):
                                None) == native.DCN_ERR_NULL
     bad = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=7)
     assert lib.dcn_core_fwd_om(ctypes.byref(bad.c()), A, A, 32, A, None) == native.DCN_ERR_DTYPE
+
+
+# ---- dcn_linear: argument errors are returned before any CUDA call ----------
+
+def _lin(native, M, K, N, dtype=None):
+    return native.dcn_linear_params_t(M, K, N, native.DCN_F16 if dtype is None else dtype)
+
+
+def test_linear_argument_errors(native):
+    import ctypes
+    L = native.lib()
+    good = 0x10000  # any 16-byte aligned address; nothing is dereferenced on error
+    assert L.dcn_linear(None, good, good, None, good, None) == native.DCN_ERR_NULL
+    assert L.dcn_linear(ctypes.byref(_lin(native, 4, 64, 16, 7)), good, good, None, good,
+                        None) == native.DCN_ERR_DTYPE
+    for M, K, N in ((-1, 64, 16), (4, 0, 16), (4, 64, 0)):
+        assert L.dcn_linear(ctypes.byref(_lin(native, M, K, N)), good, good, None, good,
+                            None) == native.DCN_ERR_SHAPE
+    assert L.dcn_linear(ctypes.byref(_lin(native, 4, 64, 16)), None, good, None, good,
+                        None) == native.DCN_ERR_NULL
+    assert L.dcn_linear(ctypes.byref(_lin(native, 4, 64, 16)), good + 1, good, None, good,
+                        None) == native.DCN_ERR_ALIGN
+    assert L.dcn_linear(ctypes.byref(_lin(native, 4, 64, 16)), good, good, good + 1, good,
+                        None) == native.DCN_ERR_ALIGN
+    # no rows: nothing to do, and nothing is touched
+    assert L.dcn_linear(ctypes.byref(_lin(native, 0, 64, 16)), None, None, None, None, None) == native.DCN_OK
