@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
@@ -66,6 +67,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
+// 16 columns of one tensor-memory lane per thread, without waiting: the
+// caller issues several, then one tcgen05.wait::ld
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -80,21 +93,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// x (M, K) and w (N, K) through the tensor maps (boxes of 64 x 128 rows and
-// 64 x N rows, 128-byte swizzle); K = 64 * KB, 16 <= N <= 256, N % 16 == 0.
-// Dynamic shared memory: 1024 bytes of alignment slack, KB x [128 x 128 B] of
-// x, KB x [N x 128 B] of w, then two barriers and the tensor-memory address.
+// x (M, K), w (N, K) and y (M, N) through tensor maps with boxes of 64
+// columns (128 bytes, 128-byte swizzle) by 128 rows (x, y) or N rows (w);
+// K = 64 * KB, N a multiple of 16 up to 256 (the store clips the last block
+// at N).  Dynamic shared memory: 1024 bytes of alignment slack, then
+// KB x [128 x 128 B] of x and KB x [N x 128 B] of w (later the staging blocks
+// of y), then two barriers and the tensor-memory address.
 template <typename T>
 __global__ void __launch_bounds__(128)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
-                 int M, int N, int KB, int tcols, const T* __restrict__ bias, T* __restrict__ y) {
+                 const __grid_constant__ CUtensorMap ymap, int M, int N, int KB, int tcols,
+                 const T* __restrict__ bias) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled layout is defined on 1024-byte aligned addresses
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   unsigned char* xs = smem;
   unsigned char* ws = smem + KB * 128 * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ws + KB * N * 128);  // [0] copies, [1] MMA
+  // after the MMAs the operand tiles are free: the output is staged there,
+  // one 128-row x 64-column (128-byte) swizzled block per 64 outputs
+  unsigned char* ys = smem;
+  const int opnd = KB * (128 + N) * 128, stage = 128 * ((N + 63) / 64) * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (opnd > stage ? opnd : stage));
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * 128;
@@ -155,8 +175,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
   if (ok) {
-    // warp w holds rows 32w .. 32w + 31 of the tile in tensor-memory lanes
-    const int row = m0 + warp * 32 + lane;
+    // warp w holds rows 32w .. 32w + 31 of the tile in tensor-memory lanes;
+    // each thread writes its row into the staging blocks (16-byte chunk j of
+    // row r at chunk j ^ (r & 7), the layout the store's swizzle reads), then
+    // one thread stores each 64-column block with a tensor copy, which clips
+    // rows past M
+    const int r = warp * 32 + lane;
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
     for (int c = 0; c < N; c += 16) {
       float v[16];
@@ -165,14 +189,29 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] += to_f32(bias[c + i]);
       }
-      if (row < M) {
-        uint32_t wv[8];
+      uint32_t wv[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wv[i] = Dt<T>::pack(v + 2 * i);
-        uint4* dst = reinterpret_cast<uint4*>(y + (size_t)row * N + c);
-        dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-        dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-      }
+      for (int i = 0; i < 8; ++i) wv[i] = Dt<T>::pack(v + 2 * i);
+      unsigned char* blk = ys + (c >> 6) * (128 * 128) + r * 128;
+      const int j0 = (c & 63) >> 3;  // first 16-byte chunk of these 16 columns
+      *reinterpret_cast<uint4*>(blk + (((j0) ^ (r & 7)) << 4)) =
+          make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      *reinterpret_cast<uint4*>(blk + (((j0 + 1) ^ (r & 7)) << 4)) =
+          make_uint4(wv[4], wv[5], wv[6], wv[7]);
+    }
+    // the generic-proxy writes above become visible to the tensor copy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < N; c += 64)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::
+                "l"(reinterpret_cast<uint64_t>(&ymap)),
+            "r"(c), "r"(m0), "r"(smem_addr(ys + (c >> 6) * (128 * 128)))
+            : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      // the block's shared memory must outlive the copies' reads of it
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
   } else if (threadIdx.x == 0) {
     atomicAdd(&g_linear_wait_timeouts, 1ull);
@@ -186,6 +225,216 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   if (warp == 0) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tcols)
+                 : "memory");
+  }
+}
+
+// ---- the persistent, warp-specialised version ---------------------------------
+// One CTA per SM walks the 128-row tiles t = blockIdx.x + i * gridDim.x:
+//   warp 0 (one lane): the producer.  W once into shared memory, then the x
+//     tiles into a ring of S stages (full / empty barriers per stage);
+//   warp 1 (one lane): the MMA issuer.  Per tile, the tcgen05.mma chain into
+//     one of two tensor-memory accumulators, then commits that free the x stage
+//     and announce the accumulator;
+//   warps 2-9: the epilogue.  Each reads a quarter of the accumulator's 128
+//     lanes (warp w: lanes 32 * (w % 4) ...) for half of its columns, frees
+//     the accumulator, adds the bias (staged once in shared memory), writes
+//     the staging block of its buffer (two, alternating), and one thread
+//     stores the tile with tensor copies while the next tile's MMAs run.
+// All waits are bounded.  A role whose wait runs out raises the block's
+// abort flag; the others see it in their own waits and stop; the epilogue
+// warps decide together (a barrier reduction), so none is left at a barrier.
+struct LinearWs {
+  int S;          // x stages
+  int ntiles;     // ceil(M / 128)
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort) {
+  for (int i = 0; i < kLinearWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(320, 1)
+linear_ws_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                 const __grid_constant__ CUtensorMap ymap, int N, int KB, int tcols, int S,
+                 int YB, int ntiles, const T* __restrict__ bias) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int ystage = 128 * ((N + 63) / 64) * 128;  // one staging buffer
+  unsigned char* ws = smem;                          // KB x N x 128 B
+  unsigned char* as = ws + KB * N * 128;             // S x KB x 16 KB
+  unsigned char* ys = as + S * KB * 128 * 128;       // YB x ystage (1 or 2)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ys + YB * ystage);
+  uint64_t* wfull = bars;                            // 1
+  uint64_t* afull = bars + 1;                        // S
+  uint64_t* aempty = afull + S;                      // S
+  uint64_t* tfull = aempty + S;                      // 2
+  uint64_t* tempty = tfull + 2;                      // 2
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+  float* sbias = reinterpret_cast<float*>(tslot + 4);  // N
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tslot)),
+                 "r"(2 * tcols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    mbar_init(wfull, 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);
+    }
+    *abort = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer
+    mbar_expect_tx(wfull, (uint32_t)(KB * N * 128));
+    for (int kb = 0; kb < KB; ++kb) tma_load_2d(ws + kb * N * 128, &wmap, wfull, kb * 64, 0);
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int st = i % S;
+      if (!wait_or_abort(&aempty[st], ((i / S) & 1) ^ 1, abort)) break;
+      mbar_expect_tx(&afull[st], (uint32_t)(KB * 128 * 128));
+      for (int kb = 0; kb < KB; ++kb)
+        tma_load_2d(as + (st * KB + kb) * 128 * 128, &xmap, &afull[st], kb * 64, t * 128);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t idesc = mma_idesc(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u,
+                                     (uint32_t)N, 128u);
+    if (wait_or_abort(wfull, 0, abort)) {
+      int i = 0;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        const int st = i % S, b = i & 1;
+        if (!wait_or_abort(&afull[st], (i / S) & 1, abort)) break;
+        if (!wait_or_abort(&tempty[b], ((i >> 1) & 1) ^ 1, abort)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = tmem + (uint32_t)(b * tcols);
+        for (int kb = 0; kb < KB; ++kb) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_desc(smem_addr(as + (st * KB + kb) * 128 * 128) + 32u * kk);
+            const uint64_t bd = sw128_desc(smem_addr(ws + kb * N * 128) + 32u * kk);
+            const uint32_t acc = (kb | kk) != 0;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+                : "memory");
+          }
+        }
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&aempty[st]))
+            : "memory");
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&tfull[b]))
+            : "memory");
+      }
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) ... for the
+    // columns of half (w - 2) / 4
+    const int q = warp & 3, r = q * 32 + lane, half = (warp - 2) >> 2;
+    const int et = threadIdx.x - 64;
+    const bool leader = et == 0;
+    const int c0 = half * (N >> 1), c1 = c0 + (N >> 1);
+    for (int c = et; c < N; c += 256) sbias[c] = bias ? to_f32(bias[c]) : 0.f;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const bool ok = wait_or_abort(&tfull[b], (i >> 1) & 1, abort);
+      // all eight warps stop together if any wait ran out
+      uint32_t bad;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(bad)
+          : "r"(ok ? 0 : 1)
+          : "memory");
+      if (bad) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      // the staging buffer was last stored YB tiles ago: its copy must have
+      // read it (with two buffers the previous tile's copy may still read)
+      if (leader && i >= YB) {
+        if (YB == 2)
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      unsigned char* yb = ys + (YB == 2 ? b : 0) * ystage;
+      const uint32_t tbase = tmem + (uint32_t)(b * tcols) + ((uint32_t)(q * 32) << 16);
+      for (int c = c0; c < c1; c += 32) {
+        // two loads in flight, one wait
+        uint32_t ra[16], rb[16];
+        tmem_ld16_async(tbase + (uint32_t)c, ra);
+        tmem_ld16_async(tbase + (uint32_t)(c + 16), rb);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t* rr = hh ? rb : ra;
+          const int cc = c + 16 * hh;
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(rr[e]) + sbias[cc + e];
+          uint32_t wv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wv[e] = Dt<T>::pack(v + 2 * e);
+          unsigned char* blk = yb + (cc >> 6) * (128 * 128) + r * 128;
+          const int j0 = (cc & 63) >> 3;
+          *reinterpret_cast<uint4*>(blk + ((j0 ^ (r & 7)) << 4)) =
+              make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          *reinterpret_cast<uint4*>(blk + (((j0 + 1) ^ (r & 7)) << 4)) =
+              make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        }
+      }
+      // the accumulator is read: the MMA of tile i + 2 may overwrite it
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (leader) {
+        for (int c = 0; c < N; c += 64)
+          asm volatile(
+              "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::
+                  "l"(reinterpret_cast<uint64_t>(&ymap)),
+              "r"(c), "r"(t * 128), "r"(smem_addr(yb + (c >> 6) * (128 * 128)))
+              : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    }
+    if (leader) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) atomicAdd(&g_linear_wait_timeouts, 1ull);
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(2 * tcols)
                  : "memory");
   }
 }
@@ -207,6 +456,17 @@ linear_simt_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
 }
 
 // ---- host side ------------------------------------------------------------------
+
+static int env_int_dev(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  return v && *v ? std::atoi(v) : dflt;
+}
+
+static int dev_of_stream() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
 
 static PFN_cuTensorMapEncodeTiled_v12000 linear_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -238,7 +498,30 @@ static bool encode_rows(CUtensorMap* m, int dtype, const void* base, long long r
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t linear_tc_smem(int K, int N) { return 1024 + (size_t)(K / 64) * (128 + N) * 128 + 32; }
+// Shared memory of the persistent kernel with S x stages and YB output
+// staging buffers (two if they fit, else one; 0 when not even S = 2, YB = 1
+// fits in 227 KB).
+static size_t linear_ws_smem(int K, int N, int* S_out, int* YB_out) {
+  const size_t KB = K / 64, w = KB * N * 128, a = KB * 128 * 128,
+               y = (size_t)128 * ((N + 63) / 64) * 128,
+               bars = 8 * (1 + 2 * 4 + 4) + 16 + 4 * (size_t)N;
+  for (int YB = 2; YB >= 1; --YB)
+    for (int S = 4; S >= 2; --S) {
+      const size_t total = 1024 + w + S * a + YB * y + bars;
+      if (total <= 227 * 1024) {
+        *S_out = S;
+        *YB_out = YB;
+        return total;
+      }
+    }
+  return 0;
+}
+
+size_t linear_tc_smem(int K, int N) {
+  const size_t opnd = (size_t)(K / 64) * (128 + N) * 128,
+               stage = (size_t)128 * ((N + 63) / 64) * 128;
+  return 1024 + (opnd > stage ? opnd : stage) + 32;
+}
 
 bool linear_tc_ok(int dtype, long long M, int K, int N, const void* x, const void* w,
                   const void* y) {
@@ -257,17 +540,33 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
   T* y_ = static_cast<T*>(y);
   if constexpr (sizeof(T) == 2) {
     if (tc) {
-      CUtensorMap xm, wm;
-      if (!encode_rows(&xm, dtype, x, M, K, 128) || !encode_rows(&wm, dtype, w, N, K, N))
+      CUtensorMap xm, wm, ym;
+      if (!encode_rows(&xm, dtype, x, M, K, 128) || !encode_rows(&wm, dtype, w, N, K, N) ||
+          !encode_rows(&ym, dtype, y, M, N, 128))
         return cudaErrorInvalidValue;
       int tcols = 32;
       while (tcols < N) tcols <<= 1;
+      int S = 0, YB = 0;
+      const size_t wsm = linear_ws_smem(K, N, &S, &YB);
+      if (wsm && 2 * tcols <= 512 && N % 64 == 0 && env_int_dev("DCN_LINEAR_PERSIST", 1)) {
+        cudaError_t e = cudaFuncSetAttribute(linear_ws_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_of_stream());
+        if (e != cudaSuccess) return e;
+        const int ntiles = (int)((M + 127) / 128);
+        const int grid = ntiles < sms ? ntiles : sms;
+        linear_ws_kernel<T><<<grid, 320, wsm, s>>>(xm, wm, ym, N, K / 64, tcols, S, YB, ntiles,
+                                                   b_);
+        return cudaGetLastError();
+      }
       const size_t smem = linear_tc_smem(K, N);
       cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<T>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       const unsigned grid = (unsigned)((M + 127) / 128);
-      linear_tc_kernel<T><<<grid, 128, smem, s>>>(xm, wm, (int)M, N, K / 64, tcols, b_, y_);
+      linear_tc_kernel<T><<<grid, 128, smem, s>>>(xm, wm, ym, (int)M, N, K / 64, tcols, b_);
       return cudaGetLastError();
     }
   }
