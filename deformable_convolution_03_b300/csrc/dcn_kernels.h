@@ -63,9 +63,9 @@ cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& 
 // Blocks whose bounded wait for a tensor copy ran out, since load.
 cudaError_t read_wait_timeouts(unsigned long long* count);
 
-// The linear projections (dcn_linear.cu): the tensor-core kernel when tc
-// (the shape and alignment checks of linear_tc_ok pass), else one thread per
-// output element.
+// The linear projections (dcn_linear.cu): the tensor-core kernels when tc
+// (the shape and alignment checks of linear_tc_ok pass), else shared-memory
+// tiles on the CUDA cores.
 bool linear_tc_ok(int dtype, long long M, int K, int N, const void* x, const void* w,
                   const void* y);
 cudaError_t launch_linear(int dtype, long long M, int K, int N, const void* x, const void* w,

@@ -18,8 +18,8 @@
 // not complete counts it (dcn_wait_timeouts), writes nothing, still frees its
 // tensor memory and waits once more (bounded) for what it issued.
 //
-// linear_simt_kernel: any shape and float32, one thread per output element,
-// float32 accumulation.
+// linear_simt_kernel: any shape and float32, shared-memory tiles on the CUDA
+// cores, float32 accumulation.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -439,20 +439,53 @@ linear_ws_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   }
 }
 
-// Any shape, any of the three types: one thread per output element.
+// Any shape, any of the three types: 64 x 64 output tiles per block of 256
+// threads (4 x 4 outputs each), the x and W slices of 32 channels staged in
+// shared memory, float32 accumulation.
 template <typename T>
 __global__ void __launch_bounds__(256)
 linear_simt_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __restrict__ bias,
                    T* __restrict__ y, long long M, int K, int N) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= M * N) return;
-  const long long m = i / N;
-  const int n = (int)(i - m * N);
-  const T* xr = x + m * K;
-  const T* wr = w + (size_t)n * K;
-  float acc = bias ? to_f32(bias[n]) : 0.f;
-  for (int k = 0; k < K; ++k) acc = fmaf(to_f32(xr[k]), to_f32(wr[k]), acc);
-  y[i] = Dt<T>::from_f(acc);
+  __shared__ float xs[32][65];
+  __shared__ float wsh[32][65];
+  const long long m0 = (long long)blockIdx.x * 64;
+  const int n0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      const int rr = i >> 5, kk = i & 31;
+      const long long m = m0 + rr;
+      const int n = n0 + rr, k = k0 + kk;
+      xs[kk][rr] = (m < M && k < K) ? to_f32(x[m * K + k]) : 0.f;
+      wsh[kk][rr] = (n < N && k < K) ? to_f32(w[(size_t)n * K + k]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; ++kk) {
+      float a[4], bb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        a[i] = xs[kk][ty * 4 + i];
+        bb[i] = wsh[kk][tx * 4 + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < N) y[m * N + n] = Dt<T>::from_f(acc[i][j] + (bias ? to_f32(bias[n]) : 0.f));
+    }
+  }
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -570,11 +603,10 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
       return cudaGetLastError();
     }
   }
-  const long long total = M * N;
-  const long long grid = (total + 255) / 256;
-  if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-  linear_simt_kernel<T><<<(unsigned)grid, 256, 0, s>>>(static_cast<const T*>(x),
-                                                       static_cast<const T*>(w), b_, y_, M, K, N);
+  const long long gx = (M + 63) / 64, gy = (N + 63) / 64;
+  if (gx > INT_MAX || gy > 65535) return cudaErrorInvalidConfiguration;
+  linear_simt_kernel<T><<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(
+      static_cast<const T*>(x), static_cast<const T*>(w), b_, y_, M, K, N);
   return cudaGetLastError();
 }
 

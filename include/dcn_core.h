@@ -198,7 +198,7 @@ int dcn_core_bwd_noalloc(const dcn_params_t* p, const void* grad_out, const void
  * the storage type.  For float16 / bfloat16 with K a multiple of 64 up to 256,
  * N a multiple of 16 from 16 to 256 and x, w, y 16-byte aligned, the product
  * runs on the tensor cores (tcgen05, operands staged by tensor copies);
- * otherwise one CUDA thread per output element.  M == 0 launches nothing.
+ * otherwise on the CUDA cores (shared-memory tiles).  M == 0 launches nothing.
  * DCN_ERR_NULL / DCN_ERR_SHAPE (M < 0, K < 1, N < 1) / DCN_ERR_DTYPE /
  * DCN_ERR_ALIGN (a pointer not aligned to the element size) on bad
  * arguments, before any CUDA call. */
