@@ -17,6 +17,8 @@ storage), on seeded synthetic inputs already resident in HBM.
               depth x step time of the four stages
   cpu_baseline = the oracle (plain binary64 loops) on the host cores, on a
               bounded sample of the same workload
+  projections = the dense layers around the core (offset/mask and output
+              projections, dcn_linear) at the workload's shape, beside the step
 
 L2 is flushed (a write of twice its size) before every timed step, outside
 the step's events.  ``--impl reference`` times the oracle alone, on the host.
@@ -285,6 +287,41 @@ def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
     return times, h2d, d2h
 
 
+def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
+    """The dense layers around the core at the workload's shape (dcn_linear):
+    DCNv4's merged offset/mask projection (C -> G x row stride, P = 9 rows
+    padded to 32) and the output projection (C -> C), on synthetic inputs and
+    weights, each timed alone with L2 flushed, against HBM on their ideal
+    bytes (x read, W read, y written once)."""
+    dt = DTYPES[w.dtype]
+    M, C = w.N * w.H_out * w.W_out, w.C
+    rs = 32 if w.P == 9 else ((3 * w.P + 7) // 8) * 8
+    g = torch.Generator().manual_seed(77)
+    out = {}
+    for name, n_out in (("offset_mask", w.G * rs), ("output_proj", C)):
+        x = (torch.rand(M, C, generator=g) * 2 - 1).to(dt).to(dev)
+        wt = (torch.randn(n_out, C, generator=g) / C ** 0.5).to(dt).to(dev)
+        b = torch.randn(n_out, generator=g).to(dt).to(dev)
+        for _ in range(3):
+            B.linear(x, wt, b)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            B.linear(x, wt, b)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.mean(ts)
+        es = torch.empty(0, dtype=dt).element_size()
+        ideal = (M * C + n_out * C + n_out + M * n_out) * es
+        gbs = ideal / (ms * 1e-3) / 1e9
+        out[name] = {"shape": f"{M}x{C} -> {n_out}", "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak, 4), "ideal_bytes": ideal}
+    return out
+
+
 def images_per_s(dev, flush, reps: int):
     """FlashInternImage-T core op: 64 images / sum_i depth_i * t_i (fwd, fwd+bwd)."""
     per_stage = []
@@ -407,6 +444,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle timing")
     ap.add_argument("--no-stages", action="store_true", help="skip the T-stage images/s sweep")
+    ap.add_argument("--no-proj", action="store_true",
+                    help="skip the projections around the core (dcn_linear)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     args = ap.parse_args()
@@ -500,6 +539,8 @@ def main():
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 3),
     }
+    if rank == 0 and not args.no_proj:
+        line["projections"] = projections(w, dev, flush, reps=200, peak=peak)
     if rank == 0 and not args.no_stages:
         line["images_per_s"] = images_per_s(dev, flush, reps=200)
     if rank == 0 and world == 1 and not args.no_cpu:
