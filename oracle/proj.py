@@ -17,6 +17,14 @@ then P mask values, padded to the row stride.
 Every one of those layers is y = x W^T + b over the rows of a channels-last
 tensor, which is what this module computes, in binary64, with numpy's matrix
 product as the one library step.
+
+The centre feature scale (the InternImage-G walkthrough, section 三 item 5;
+the DCNv4 guide, "高级配置参数详解") sits between the core and output_proj: a
+sigmoid gate mixes the core's output with the centre pixel's own projected
+feature x_proj.  The walkthrough gives the gate's function and inputs but not
+its shape; this module takes one gate per (pixel, group), from G logits per
+pixel (a linear layer of G outputs), applied to the group's gc channels:
+    s = 1 / (1 + exp(-logit)),   out = core * (1 - s) + x_proj * s.
 """
 from __future__ import annotations
 
@@ -64,3 +72,38 @@ def merged_weights(w_offset, b_offset, w_mask, b_mask, G: int, P: int, row_strid
         w[r + 2 * P:r + 3 * P] = w_mask[g * P:(g + 1) * P]
         b[r + 2 * P:r + 3 * P] = bm[g * P:(g + 1) * P]
     return w, b
+
+
+def _gate(logits, M, G):
+    l = np.asarray(logits, dtype=np.float64).reshape(M, G)
+    with np.errstate(over="ignore"):  # exp(-l) = inf gives the limit s = 0
+        return 1.0 / (1.0 + np.exp(-l))
+
+
+def center_feature_scale(core, x_proj, logits, G: int) -> np.ndarray:
+    """out[m, g*gc + c] = core * (1 - s[m, g]) + x_proj * s[m, g], with
+    s = sigmoid(logits[m, g]), in binary64.
+
+    core, x_proj: (M, C) rows of C = G * gc channels; logits: (M, G)."""
+    core = np.asarray(core, dtype=np.float64)
+    x = np.asarray(x_proj, dtype=np.float64)
+    M, C = core.shape
+    if x.shape != (M, C) or C % G:
+        raise ValueError("inconsistent centre-feature-scale shapes")
+    s = np.repeat(_gate(logits, M, G), C // G, axis=1)
+    return core * (1.0 - s) + x * s
+
+
+def center_feature_scale_backward(grad_out, core, x_proj, logits, G: int):
+    """The gradients of center_feature_scale, in binary64:
+    d core = g * (1 - s), d x_proj = g * s and
+    d logit[m, k] = s (1 - s) * sum over group k's channels of g * (x_proj - core)
+    (ds/dlogit = s (1 - s) for the logistic function).  Returns the three."""
+    g = np.asarray(grad_out, dtype=np.float64)
+    core = np.asarray(core, dtype=np.float64)
+    x = np.asarray(x_proj, dtype=np.float64)
+    M, C = core.shape
+    s = _gate(logits, M, G)
+    se = np.repeat(s, C // G, axis=1)
+    dl = (g * (x - core)).reshape(M, G, C // G).sum(axis=2) * s * (1.0 - s)
+    return g * (1.0 - se), g * se, dl
