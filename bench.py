@@ -17,8 +17,9 @@ storage), on seeded synthetic inputs already resident in HBM.
               depth x step time of the four stages
   cpu_baseline = the oracle (plain binary64 loops) on the host cores, on a
               bounded sample of the same workload
-  projections = the dense layers around the core (offset/mask and output
-              projections, dcn_linear) at the workload's shape, beside the step
+  projections = the layers around the core at the workload's shape, beside
+              the step: the offset/mask and output projections (dcn_linear) and
+              the centre feature scale (forward and backward)
 
 L2 is flushed (a write of twice its size) before every timed step, outside
 the step's events.  ``--impl reference`` times the oracle alone, on the host.
@@ -288,11 +289,12 @@ def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
 
 
 def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
-    """The dense layers around the core at the workload's shape (dcn_linear):
-    DCNv4's merged offset/mask projection (C -> G x row stride, P = 9 rows
-    padded to 32) and the output projection (C -> C), on synthetic inputs and
-    weights, each timed alone with L2 flushed, against HBM on their ideal
-    bytes (x read, W read, y written once)."""
+    """The layers around the core at the workload's shape: DCNv4's merged
+    offset/mask projection (C -> G x row stride, P = 9 rows padded to 32) and
+    the output projection (C -> C) by dcn_linear, and the centre feature
+    scale's mix (dcn_center_feature_scale, forward and backward), on synthetic
+    inputs and weights, each timed alone with L2 flushed, against HBM on their
+    ideal bytes (each tensor read or written once)."""
     dt = DTYPES[w.dtype]
     M, C = w.N * w.H_out * w.W_out, w.C
     rs = 32 if w.P == 9 else ((3 * w.P + 7) // 8) * 8
@@ -318,6 +320,33 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
         ideal = (M * C + n_out * C + n_out + M * n_out) * es
         gbs = ideal / (ms * 1e-3) / 1e9
         out[name] = {"shape": f"{M}x{C} -> {n_out}", "ms": round(ms, 5), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peak, 4), "ideal_bytes": ideal}
+    # the centre feature scale: its gate logits (C -> G), then the mix of the
+    # core's output with x_proj, forward and backward
+    es = torch.empty(0, dtype=dt).element_size()
+    core, xp, go = ((torch.rand(M, C, generator=g) * 2 - 1).to(dt).to(dev) for _ in range(3))
+    lg = torch.randn(M, w.G, generator=g).to(dt).to(dev)
+    gates = {
+        "cfs_forward": (lambda: B.center_feature_scale(core, xp, lg),
+                        (3 * M * C + M * w.G) * es),
+        "cfs_backward": (lambda: B.center_feature_scale_backward(go, core, xp, lg),
+                         (5 * M * C + 2 * M * w.G) * es),
+    }
+    for name, (fn, ideal) in gates.items():
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.mean(ts)
+        gbs = ideal / (ms * 1e-3) / 1e9
+        out[name] = {"shape": f"{M}x{C}, {w.G} gates", "ms": round(ms, 5), "GB/s": round(gbs, 1),
                      "frac_hbm": round(gbs / peak, 4), "ideal_bytes": ideal}
     return out
 

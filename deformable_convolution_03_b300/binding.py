@@ -32,7 +32,8 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
-           "dcn_linear", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
+           "dcn_linear", "dcn_center_feature_scale", "dcn_center_feature_scale_bwd",
+           "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -99,6 +100,9 @@ def lib() -> ctypes.CDLL:
                                       vp]
         L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
         L.dcn_linear.argtypes = [ctypes.POINTER(dcn_linear_params_t), vp, vp, vp, vp, vp]
+        L.dcn_center_feature_scale.argtypes = [ctypes.POINTER(dcn_cfs_params_t), vp, vp, vp, vp,
+                                               vp]
+        L.dcn_center_feature_scale_bwd.argtypes = [ctypes.POINTER(dcn_cfs_params_t)] + [vp] * 8
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -160,6 +164,67 @@ def linear(x, w, bias=None):
     y = torch.empty(x2.shape[0], w.shape[0], dtype=x.dtype, device=x.device)
     dcn_linear(x2, w, bias, y, torch.cuda.current_stream(x.device).cuda_stream)
     return y.reshape(*x.shape[:-1], w.shape[0])
+
+
+class dcn_cfs_params_t(ctypes.Structure):
+    """Mirror of dcn_cfs_params_t (include/dcn_core.h)."""
+    _fields_ = [("M", ctypes.c_longlong), ("C", ctypes.c_int), ("G", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+def dcn_center_feature_scale(core, x_proj, logits, out, G, stream=None) -> None:
+    """Raw entry point: out = core * (1 - s) + x_proj * s, s = sigmoid(logits)
+    per (row, group); core, x_proj, out (M, C), logits (M, G)."""
+    M, C = int(core.shape[0]), int(core.shape[1])
+    p = dcn_cfs_params_t(M, C, int(G), TORCH_TO_DCN[core.dtype])
+    _check(lib().dcn_center_feature_scale(ctypes.byref(p), _ptr(core), _ptr(x_proj),
+                                          _ptr(logits), _ptr(out), _stream(stream)),
+           "dcn_center_feature_scale")
+
+
+def dcn_center_feature_scale_bwd(grad_out, core, x_proj, logits, grad_core, grad_x_proj,
+                                 grad_logits, G, stream=None) -> None:
+    """Raw entry point: the three gradients of dcn_center_feature_scale."""
+    M, C = int(core.shape[0]), int(core.shape[1])
+    p = dcn_cfs_params_t(M, C, int(G), TORCH_TO_DCN[core.dtype])
+    _check(lib().dcn_center_feature_scale_bwd(
+        ctypes.byref(p), _ptr(grad_out), _ptr(core), _ptr(x_proj), _ptr(logits),
+        _ptr(grad_core), _ptr(grad_x_proj), _ptr(grad_logits), _stream(stream)),
+        "dcn_center_feature_scale_bwd")
+
+
+def _cfs_args(tensors, C, G):
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != tensors[0].dtype:
+            raise ValueError("center_feature_scale: contiguous CUDA tensors of one dtype expected")
+    if C % G:
+        raise ValueError(f"center_feature_scale: {C} channels do not split into {G} groups")
+
+
+def center_feature_scale(core, x_proj, logits):
+    """The centre feature scale on the GPU: core, x_proj (..., C) channels-last,
+    logits (..., G); returns core * (1 - s) + x_proj * s with s = sigmoid(logits)
+    per (pixel, group)."""
+    C, G = core.shape[-1], logits.shape[-1]
+    _cfs_args((core, x_proj, logits), C, G)
+    if x_proj.shape != core.shape or logits.shape[:-1] != core.shape[:-1]:
+        raise ValueError("center_feature_scale: shapes do not match")
+    out = torch.empty_like(core)
+    dcn_center_feature_scale(core.reshape(-1, C), x_proj.reshape(-1, C), logits.reshape(-1, G),
+                             out.reshape(-1, C), G, torch.cuda.current_stream(core.device).cuda_stream)
+    return out
+
+
+def center_feature_scale_backward(grad_out, core, x_proj, logits):
+    """The gradients (grad_core, grad_x_proj, grad_logits) of center_feature_scale."""
+    C, G = core.shape[-1], logits.shape[-1]
+    _cfs_args((grad_out, core, x_proj, logits), C, G)
+    gc, gx, gl = torch.empty_like(core), torch.empty_like(x_proj), torch.empty_like(logits)
+    dcn_center_feature_scale_bwd(grad_out.reshape(-1, C), core.reshape(-1, C),
+                                 x_proj.reshape(-1, C), logits.reshape(-1, G), gc.reshape(-1, C),
+                                 gx.reshape(-1, C), gl.reshape(-1, G), G,
+                                 torch.cuda.current_stream(core.device).cuda_stream)
+    return gc, gx, gl
 
 
 def dcn_wait_timeouts() -> int:

@@ -4,6 +4,7 @@
 // Every check runs on the host before the first CUDA call, so a rejected
 // call leaves the device untouched.  No entry point allocates memory.
 #include <algorithm>
+#include <initializer_list>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -588,6 +589,35 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
 
 }  // namespace
 
+namespace {
+
+// The widest access (16, 8, 4 bytes or one element) that divides a group's
+// bytes and to which every pointer is aligned; for the backward also with
+// gc / V a power of two <= 32 (the shuffle reduction), else 0.
+int cfs_vbytes(int gc, int es, bool bwd, std::initializer_list<const void*> ptrs) {
+  for (int vb = 16; vb >= es; vb /= 2) {
+    if ((gc * es) % vb) continue;
+    bool ok = true;
+    for (const void* q : ptrs) ok = ok && aligned(q, vb);
+    if (!ok) continue;
+    const int L = gc / (vb / es);
+    if (bwd && (L > 32 || (L & (L - 1)))) continue;
+    return vb;
+  }
+  return bwd ? 0 : es;
+}
+
+int cfs_check(const dcn_cfs_params_t* p, int* es) {
+  if (!p) return DCN_ERR_NULL;
+  *es = elem_size(p->dtype);
+  if (*es == 0) return DCN_ERR_DTYPE;
+  if (p->M < 0 || p->C < 1 || p->G < 1 || p->C % p->G) return DCN_ERR_SHAPE;
+  if (p->M >= (1LL << 40) / p->C) return DCN_ERR_UNSUPPORTED;
+  return DCN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
@@ -656,6 +686,41 @@ int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const
   if (fault_injected()) return DCN_ERR_CUDA;
   return cuda_status(dcn::launch_linear(p->dtype, p->M, p->K, p->N, x, w, bias, y, tc,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+
+int dcn_center_feature_scale(const dcn_cfs_params_t* p, const void* core, const void* x_proj,
+                             const void* logits, void* out, void* stream) {
+  int es = 0;
+  if (const int rc = cfs_check(p, &es)) return rc;
+  if (p->M == 0) return DCN_OK;
+  if (!core || !x_proj || !logits || !out) return DCN_ERR_NULL;
+  for (const void* q : {core, x_proj, logits, (const void*)out})
+    if (!aligned(q, es)) return DCN_ERR_ALIGN;
+  const int vb = cfs_vbytes(p->C / p->G, es, false, {core, x_proj, out});
+  if (fault_injected()) return DCN_ERR_CUDA;
+  return cuda_status(dcn::launch_cfs_fwd(p->dtype, vb, p->M, p->C, p->G, core, x_proj, logits,
+                                         out, static_cast<cudaStream_t>(stream)));
+}
+
+int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out,
+                                 const void* core, const void* x_proj, const void* logits,
+                                 void* grad_core, void* grad_x_proj, void* grad_logits,
+                                 void* stream) {
+  int es = 0;
+  if (const int rc = cfs_check(p, &es)) return rc;
+  if (p->M == 0) return DCN_OK;
+  if (!grad_out || !core || !x_proj || !logits || !grad_core || !grad_x_proj || !grad_logits)
+    return DCN_ERR_NULL;
+  for (const void* q : {grad_out, core, x_proj, logits, (const void*)grad_core,
+                        (const void*)grad_x_proj, (const void*)grad_logits})
+    if (!aligned(q, es)) return DCN_ERR_ALIGN;
+  const int vb = cfs_vbytes(p->C / p->G, es, true,
+                            {grad_out, core, x_proj, grad_core, grad_x_proj});
+  if (fault_injected()) return DCN_ERR_CUDA;
+  return cuda_status(dcn::launch_cfs_bwd(p->dtype, vb, p->M, p->C, p->G, grad_out, core, x_proj,
+                                         logits, grad_core, grad_x_proj, grad_logits,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

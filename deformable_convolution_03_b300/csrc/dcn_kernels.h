@@ -72,4 +72,14 @@ cudaError_t launch_linear(int dtype, long long M, int K, int N, const void* x, c
                           const void* b, void* y, bool tc, cudaStream_t s);
 cudaError_t read_linear_wait_timeouts(unsigned long long* count);
 
+// The centre feature scale (dcn_cfs.cu).  vbytes: the bytes a thread moves per
+// access (16, 8, 4 or the element size), dividing gc * es, with every pointer
+// aligned to it.  For the backward, gc / (vbytes / es) must be a power of two
+// <= 32; vbytes == 0 selects the per-(pixel, group) kernel for any gc.
+cudaError_t launch_cfs_fwd(int dtype, int vbytes, long long M, int C, int G, const void* core,
+                           const void* x, const void* logits, void* out, cudaStream_t s);
+cudaError_t launch_cfs_bwd(int dtype, int vbytes, long long M, int C, int G, const void* gout,
+                           const void* core, const void* x, const void* logits, void* gcore,
+                           void* gx, void* glogits, cudaStream_t s);
+
 }  // namespace dcn

@@ -211,6 +211,40 @@ typedef struct {
 int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const void* bias,
                void* y, void* stream);
 
+/* The centre feature scale between the core op and output_proj (page
+ * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
+ * item 5; page "DCNv4高效实践指南：掌握可变形卷积的3倍速度提升技术", section
+ * "高级配置参数详解"): a sigmoid gate mixes the core's output with the centre
+ * pixel's projected feature x_proj (the core's input at the same pixel).  One
+ * gate per (pixel, group), s = 1 / (1 + exp(-logit)), over the group's
+ * gc = C / G channels:
+ *     out = core * (1 - s) + x_proj * s
+ * and the backward
+ *     grad_core = g * (1 - s),  grad_x_proj = g * s,
+ *     grad_logits = s (1 - s) * sum over the group's channels of g * (x_proj - core).
+ *   core, x_proj, out, grad_out, grad_core, grad_x_proj   (M, C) row-major
+ *   logits, grad_logits                                    (M, G) row-major
+ * M rows (pixels, N * Ho * Wo), C = G * gc channels, one dtype for all.
+ * Arithmetic in float32, one rounding to the storage type (the logit gradient
+ * sums its gc products in float32).  out may be the same buffer as core or as
+ * x_proj, and grad_core the same as grad_out (in place); other overlaps are
+ * not allowed.  Outputs are fully overwritten; M == 0 launches nothing.
+ * DCN_ERR_NULL / DCN_ERR_SHAPE (M < 0, C < 1, G < 1, C % G != 0) /
+ * DCN_ERR_DTYPE / DCN_ERR_ALIGN (a pointer not aligned to the element size)
+ * / DCN_ERR_UNSUPPORTED (M * C >= 2^40) before any CUDA call. */
+typedef struct {
+  long long M;  /* rows */
+  int C, G;     /* channels per row, groups */
+  int dtype;    /* dcn_dtype_t of every tensor */
+} dcn_cfs_params_t;
+
+int dcn_center_feature_scale(const dcn_cfs_params_t* p, const void* core, const void* x_proj,
+                             const void* logits, void* out, void* stream);
+int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out,
+                                 const void* core, const void* x_proj, const void* logits,
+                                 void* grad_core, void* grad_x_proj, void* grad_logits,
+                                 void* stream);
+
 /* Diagnostics of the asynchronous tensor copies some kernels use: the number
  * of thread blocks, since the library was loaded, whose bounded wait for such a
  * copy ran out on the current device.  Such a block computed its results from

@@ -207,3 +207,35 @@ def test_linear_argument_errors(native):
                         None) == native.DCN_ERR_ALIGN
     # no rows: nothing to do, and nothing is touched
     assert L.dcn_linear(ctypes.byref(_lin(native, 0, 64, 16)), None, None, None, None, None) == native.DCN_OK
+
+
+# ---- the centre feature scale: argument errors before any CUDA call ----------
+
+def _cfs(native, M, C, G, dtype=None):
+    return native.dcn_cfs_params_t(M, C, G, native.DCN_F16 if dtype is None else dtype)
+
+
+def test_centre_feature_scale_argument_errors(native):
+    import ctypes
+    L = native.lib()
+    good = 0x10000
+    f, b = L.dcn_center_feature_scale, L.dcn_center_feature_scale_bwd
+    assert f(None, good, good, good, good, None) == native.DCN_ERR_NULL
+    assert b(None, *([good] * 7), None) == native.DCN_ERR_NULL
+    assert f(ctypes.byref(_cfs(native, 4, 64, 4, 9)), good, good, good, good,
+             None) == native.DCN_ERR_DTYPE
+    for M, C, G in ((-1, 64, 4), (4, 0, 4), (4, 64, 0), (4, 64, 5)):
+        p = ctypes.byref(_cfs(native, M, C, G))
+        assert f(p, good, good, good, good, None) == native.DCN_ERR_SHAPE
+        assert b(p, *([good] * 7), None) == native.DCN_ERR_SHAPE
+    assert f(ctypes.byref(_cfs(native, 1 << 34, 64, 4)), good, good, good, good,
+             None) == native.DCN_ERR_UNSUPPORTED
+    p = ctypes.byref(_cfs(native, 4, 64, 4))
+    assert f(p, good, None, good, good, None) == native.DCN_ERR_NULL
+    assert b(p, good, good, good, good, good, None, good, None) == native.DCN_ERR_NULL
+    assert f(p, good, good + 1, good, good, None) == native.DCN_ERR_ALIGN
+    assert b(p, good, good, good, good, good, good, good + 1, None) == native.DCN_ERR_ALIGN
+    # no rows: nothing to do, and nothing is touched
+    p0 = ctypes.byref(_cfs(native, 0, 64, 4))
+    assert f(p0, None, None, None, None, None) == native.DCN_OK
+    assert b(p0, *([None] * 7), None) == native.DCN_OK
