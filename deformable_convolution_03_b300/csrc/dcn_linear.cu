@@ -439,6 +439,222 @@ linear_ws_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   }
 }
 
+// ---- any K and N: the K loop through a ring of (x, W) chunk stages -----------
+// The same roles as linear_ws_kernel, for layers whose W does not fit in
+// shared memory (K > 256 or N > 256, e.g. InternImage-G's 512 -> 512
+// projections).  Output tiles are 128 rows x BN columns (BN = 64, 128 or 256
+// dividing N), walked n-tile fastest so that the tiles of one row block reuse
+// its x chunks from L2.  Per tile the producer streams KB chunks of 64
+// channels, each an x block (128 x 128 B) and a W block (BN x 128 B), through
+// S stages; the MMA issuer consumes a stage with four K = 16 MMAs and frees it
+// by a commit; the last chunk's commit announces the accumulator.
+template <typename T>
+__global__ void __launch_bounds__(320, 1)
+linear_kloop_kernel(const __grid_constant__ CUtensorMap xmap,
+                    const __grid_constant__ CUtensorMap wmap,
+                    const __grid_constant__ CUtensorMap ymap, int BN, int KB, int S, int YB,
+                    int ntn, int ntiles, const T* __restrict__ bias, T* __restrict__ y, int M,
+                    int N) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int abytes = 128 * 128, bbytes = BN * 128, sbytes = abytes + bbytes;
+  const int ystage = 128 * BN * 2;                   // one staging buffer
+  unsigned char* st_base = smem;                     // S x (x block, W block)
+  unsigned char* ys = st_base + S * sbytes;          // YB x ystage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ys + YB * ystage);
+  uint64_t* afull = bars;                            // S
+  uint64_t* aempty = afull + S;                      // S
+  uint64_t* tfull = aempty + S;                      // 2
+  uint64_t* tempty = tfull + 2;                      // 2
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+  float* sbias = reinterpret_cast<float*>(tslot + 4);  // N
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tslot)),
+                 "r"(2 * BN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);
+    }
+    *abort = 0;
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tslot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: chunk c of the CTA's sequence goes to stage c % S
+    int c = 0;
+    bool go = true;
+    for (int t = blockIdx.x; go && t < ntiles; t += gridDim.x) {
+      const int m0 = (t / ntn) * 128, n0 = (t % ntn) * BN;
+      for (int kb = 0; kb < KB; ++kb, ++c) {
+        const int st = c % S;
+        if (!wait_or_abort(&aempty[st], ((c / S) & 1) ^ 1, abort)) {
+          go = false;
+          break;
+        }
+        unsigned char* a = st_base + st * sbytes;
+        mbar_expect_tx(&afull[st], (uint32_t)sbytes);
+        tma_load_2d(a, &xmap, &afull[st], kb * 64, m0);
+        tma_load_2d(a + abytes, &wmap, &afull[st], kb * 64, n0);
+      }
+    }
+    // no copy into this block's memory outlives it: wait (bounded) for the
+    // last chunk issued into each stage (at once when the MMAs consumed it)
+    for (int st = 0; st < S && st < c; ++st) {
+      const int last = st + ((c - 1 - st) / S) * S;
+      mbar_wait_bounded(&afull[st], (last / S) & 1, kLinearWaitPolls);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    const uint32_t idesc = mma_idesc(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u,
+                                     (uint32_t)BN, 128u);
+    int c = 0, i = 0;
+    bool go = true;
+    for (int t = blockIdx.x; go && t < ntiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      if (!wait_or_abort(&tempty[b], ((i >> 1) & 1) ^ 1, abort)) break;
+      const uint32_t d = tmem + (uint32_t)(b * BN);
+      for (int kb = 0; kb < KB; ++kb, ++c) {
+        const int st = c % S;
+        if (!wait_or_abort(&afull[st], (c / S) & 1, abort)) {
+          go = false;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a = smem_addr(st_base + st * sbytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sw128_desc(a + 32u * kk);
+          const uint64_t bd = sw128_desc(a + (uint32_t)abytes + 32u * kk);
+          const uint32_t acc = (kb | kk) != 0;
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+              "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+              : "memory");
+        }
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                smem_addr(&aempty[st]))
+            : "memory");
+      }
+      if (!go) break;
+      asm volatile(
+          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+              smem_addr(&tfull[b]))
+          : "memory");
+    }
+    // the MMAs issued are complete before the tensor memory is freed: the
+    // last commit tracks all of them (bounded)
+    if (c > 0) mbar_wait_bounded(&aempty[(c - 1) % S], ((c - 1) / S) & 1, kLinearWaitPolls);
+  } else if (warp >= 2) {
+    // ---- epilogue, as in linear_ws_kernel, for a BN-column tile at n0
+    const int q = warp & 3, r = q * 32 + lane, half = (warp - 2) >> 2;
+    const bool leader = threadIdx.x == 64;
+    const int c0 = half * (BN >> 1), c1 = c0 + (BN >> 1);
+    for (int c = threadIdx.x - 64; c < N; c += 256) sbias[c] = bias ? to_f32(bias[c]) : 0.f;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    int i = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+      const int m0 = (t / ntn) * 128, n0 = (t % ntn) * BN;
+      const int b = i & 1;
+      const bool ok = wait_or_abort(&tfull[b], (i >> 1) & 1, abort);
+      uint32_t bad;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(bad)
+          : "r"(ok ? 0 : 1)
+          : "memory");
+      if (bad) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (leader && YB > 0 && i >= YB) {
+        if (YB == 2)
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        else
+          asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+      if (YB > 0) asm volatile("bar.sync 1, 256;" ::: "memory");
+      unsigned char* yb = ys + (YB == 2 ? b : 0) * ystage;
+      const uint32_t tbase = tmem + (uint32_t)(b * BN) + ((uint32_t)(q * 32) << 16);
+      T* yrow = y + (size_t)(m0 + r) * N + n0;  // YB == 0: this thread's row
+      for (int c = c0; c < c1; c += 32) {
+        uint32_t ra[16], rb[16];
+        tmem_ld16_async(tbase + (uint32_t)c, ra);
+        tmem_ld16_async(tbase + (uint32_t)(c + 16), rb);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t* rr = hh ? rb : ra;
+          const int cc = c + 16 * hh;
+          float v[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            v[e] = __uint_as_float(rr[e]) + sbias[n0 + cc + e];
+          uint32_t wv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wv[e] = Dt<T>::pack(v + 2 * e);
+          if (YB == 0) {
+            // straight to memory: 32 contiguous bytes of the row, rows past M
+            // skipped
+            if (m0 + r < M) {
+              uint4* dst = reinterpret_cast<uint4*>(yrow + cc);
+              dst[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+              dst[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+            }
+          } else {
+            unsigned char* blk = yb + (cc >> 6) * (128 * 128) + r * 128;
+            const int j0 = (cc & 63) >> 3;
+            *reinterpret_cast<uint4*>(blk + ((j0 ^ (r & 7)) << 4)) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            *reinterpret_cast<uint4*>(blk + (((j0 + 1) ^ (r & 7)) << 4)) =
+                make_uint4(wv[4], wv[5], wv[6], wv[7]);
+          }
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      if (YB == 0) continue;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (leader) {
+        for (int c = 0; c < BN; c += 64)
+          asm volatile(
+              "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::
+                  "l"(reinterpret_cast<uint64_t>(&ymap)),
+              "r"(n0 + c), "r"(m0), "r"(smem_addr(yb + (c >> 6) * (128 * 128)))
+              : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    }
+    if (leader && YB > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) atomicAdd(&g_linear_wait_timeouts, 1ull);
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(2 * BN)
+                 : "memory");
+  }
+}
+
 // Any shape, any of the three types: 64 x 64 output tiles per block of 256
 // threads (4 x 4 outputs each), the x and W slices of 32 channels staged in
 // shared memory, float32 accumulation.
@@ -550,6 +766,35 @@ static size_t linear_ws_smem(int K, int N, int* S_out, int* YB_out) {
   return 0;
 }
 
+// The K-loop kernel's output tile width: 256, 128 or 64 columns dividing N
+// (DCN_LINEAR_BN caps it).
+static int linear_kloop_bn(int N) {
+  const int cap = env_int_dev("DCN_LINEAR_BN", 256);
+  for (int bn = 256; bn >= 64; bn >>= 1)
+    if (bn <= cap && N % bn == 0) return bn;
+  return 0;
+}
+
+// Shared memory of the K-loop kernel: S stages of (x, W) chunks, YB output
+// staging buffers and the bias, the deepest pipeline first.  YB = 0 (rows
+// stored straight from registers, DCN_LINEAR_YB=0) frees the staging memory
+// for stages but measured slower (131072 x 512 -> 512: 96 us against 82 us).
+static size_t linear_kloop_smem(int BN, int N, int* S_out, int* YB_out) {
+  const size_t sb = (size_t)(128 + BN) * 128, y = (size_t)128 * BN * 2;
+  const int ybmax = env_int_dev("DCN_LINEAR_YB", 2), smax = env_int_dev("DCN_LINEAR_S", 8);
+  const int ybmin = ybmax == 0 ? 0 : 1;
+  for (int S = smax; S >= 2; --S)
+    for (int YB = ybmax; YB >= ybmin; --YB) {
+      const size_t total = 1024 + S * sb + YB * y + 8 * (2 * S + 4) + 16 + 4 * (size_t)N;
+      if (total <= 227 * 1024) {
+        *S_out = S;
+        *YB_out = YB;
+        return total;
+      }
+    }
+  return 0;
+}
+
 size_t linear_tc_smem(int K, int N) {
   const size_t opnd = (size_t)(K / 64) * (128 + N) * 128,
                stage = (size_t)128 * ((N + 63) / 64) * 128;
@@ -559,10 +804,16 @@ size_t linear_tc_smem(int K, int N) {
 bool linear_tc_ok(int dtype, long long M, int K, int N, const void* x, const void* w,
                   const void* y) {
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  return (dtype == DCN_F16 || dtype == DCN_BF16) && M >= 1 && K % 64 == 0 && K >= 64 &&
-         K <= 256 && N % 16 == 0 && N >= 16 && N <= 256 && a16(x) && a16(w) && a16(y) &&
-         M <= (long long)INT_MAX - 128 && linear_tc_smem(K, N) <= 200 * 1024 &&
-         linear_encoder() != nullptr;
+  if (!(dtype == DCN_F16 || dtype == DCN_BF16) || M < 1 || K % 64 || K < 64 || N % 16 ||
+      N < 16 || !a16(x) || !a16(w) || !a16(y) || M > (long long)INT_MAX - 128 ||
+      linear_encoder() == nullptr)
+    return false;
+  if (K <= 256 && N <= 256) return linear_tc_smem(K, N) <= 200 * 1024;
+  // the K-loop kernel: whole 64-column output blocks, tiles counted in int
+  const int bn = linear_kloop_bn(N);
+  int S = 0, YB = 0;
+  return bn > 0 && (M + 127) / 128 * (N / bn) <= INT_MAX &&
+         linear_kloop_smem(bn, N, &S, &YB) != 0;
 }
 
 template <typename T>
@@ -572,6 +823,28 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
   const T* b_ = static_cast<const T*>(b);
   T* y_ = static_cast<T*>(y);
   if constexpr (sizeof(T) == 2) {
+    if (tc && (K > 256 || N > 256)) {
+      const int BN = linear_kloop_bn(N);
+      int S = 0, YB = 0;
+      const size_t smem = BN ? linear_kloop_smem(BN, N, &S, &YB) : 0;
+      if (!smem) return cudaErrorInvalidValue;
+      CUtensorMap xm, wm, ym;
+      if (!encode_rows(&xm, dtype, x, M, K, 128) || !encode_rows(&wm, dtype, w, N, K, BN) ||
+          !encode_rows(&ym, dtype, y, M, N, 128))
+        return cudaErrorInvalidValue;
+      cudaError_t e = cudaFuncSetAttribute(linear_kloop_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_of_stream());
+      if (e != cudaSuccess) return e;
+      const int ntn = N / BN;
+      const int ntiles = (int)((M + 127) / 128) * ntn;
+      const int grid = ntiles < sms ? ntiles : sms;
+      linear_kloop_kernel<T><<<grid, 320, smem, s>>>(xm, wm, ym, BN, K / 64, S, YB, ntn, ntiles,
+                                                     b_, y_, (int)M, N);
+      return cudaGetLastError();
+    }
     if (tc) {
       CUtensorMap xm, wm, ym;
       if (!encode_rows(&xm, dtype, x, M, K, 128) || !encode_rows(&wm, dtype, w, N, K, N) ||

@@ -195,10 +195,11 @@ int dcn_core_bwd_noalloc(const dcn_params_t* p, const void* grad_out, const void
  *   bias  (N)     or NULL, read
  *   y     (M, N)  row-major, fully overwritten
  * One dtype for all four.  Arithmetic: float32 accumulation, one rounding to
- * the storage type.  For float16 / bfloat16 with K a multiple of 64 up to 256,
- * N a multiple of 16 from 16 to 256 and x, w, y 16-byte aligned, the product
- * runs on the tensor cores (tcgen05, operands staged by tensor copies);
- * otherwise on the CUDA cores (shared-memory tiles).  M == 0 launches nothing.
+ * the storage type.  For float16 / bfloat16 with K a multiple of 64, x, w, y
+ * 16-byte aligned and N a multiple of 16 from 16 to 256 (K up to 256) or a
+ * multiple of 64 (any K), the product runs on the tensor cores (tcgen05,
+ * operands staged by tensor copies); otherwise on the CUDA cores
+ * (shared-memory tiles).  M == 0 launches nothing.
  * DCN_ERR_NULL / DCN_ERR_SHAPE (M < 0, K < 1, N < 1) / DCN_ERR_DTYPE /
  * DCN_ERR_ALIGN (a pointer not aligned to the element size) on bad
  * arguments, before any CUDA call. */

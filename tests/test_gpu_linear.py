@@ -61,6 +61,35 @@ def test_tensor_core_shapes(dt, M, K, N, bias):
     _check(M, K, N, dt, bias)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("M", [1, 129, 1000])
+@pytest.mark.parametrize("K,N", [(320, 64), (512, 512), (1024, 128), (128, 320), (64, 768),
+                                 (512, 1024)])
+def test_tensor_core_k_loop_shapes(dt, M, K, N):
+    # layers whose W does not fit in shared memory: the K loop through (x, W)
+    # chunk stages, output tiles of 64 to 256 columns, ragged row counts
+    _check(M, K, N, dt)
+
+
+@pytest.mark.parametrize("bn", ["64", "128"])
+def test_tensor_core_k_loop_narrow_tiles(bn, monkeypatch):
+    # the same layer with its output split into 64- or 128-column tiles
+    monkeypatch.setenv("DCN_LINEAR_BN", bn)
+    _check(300, 512, 512, "bf16")
+
+
+def test_full_size_projection_at_g_stage1():
+    # InternImage-G stage 1's 512 -> 512 projections on 2 x 128 x 128 pixels,
+    # checked at sampled rows
+    M, K, N = 2 * 128 * 128, 512, 512
+    x, w, b = _data(M, K, N, "bf16")
+    y = B.linear(x.cuda(), w.cuda(), b.cuda())
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(1).choice(M, 2048, replace=False)
+    ref = proj.linear(f64(x[rows]), f64(w), f64(b))
+    assert_close(y[torch.from_numpy(rows).cuda()], ref, "bf16", "projection rows")
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("K,N", [(37, 13), (64, 16), (8, 300), (512, 96)])
 def test_cuda_core_path(dt, K, N, monkeypatch):
