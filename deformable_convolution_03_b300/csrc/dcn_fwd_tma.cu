@@ -58,7 +58,9 @@ __device__ __forceinline__ void unrotate_acc_t(float (&acc)[CPT], int rot) {
   }
 }
 
-template <typename T, int CPT, int KP>
+// RB: the bytes of one window pixel (GB * gc * sizeof(T)) when known at compile
+// time (128, the usual case), else 0.
+template <typename T, int CPT, int KP, int RB>
 __global__ void __launch_bounds__(256)
 fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, const TileGeom tg,
                 const T* __restrict__ input, const T* __restrict__ offset,
@@ -136,7 +138,8 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
 #pragma unroll
     for (int i = 0; i < CPT; ++i) acc[i] = 0.f;
     // this thread's slice inside a window pixel, and the pixel's size
-    const uint32_t rb = (uint32_t)(tg.GB * kp.gc) * (uint32_t)sizeof(T);
+    const uint32_t rb = RB > 0 ? (uint32_t)RB : (uint32_t)(tg.GB * kp.gc) * (uint32_t)sizeof(T);
+    const uint32_t wrb = (uint32_t)tg.WW * rb;  // one window row
     const uint32_t chunk0 = (uint32_t)(gl * kp.gc + c0) * (uint32_t)sizeof(T) / 16u;
     // A 16-byte shared load is served eight lanes at a time: the lanes of two
     // (or four) tile pixels.  Their window pixels are unrelated, so reading
@@ -147,7 +150,6 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
     uint32_t coff[NC];  // byte offset in a window pixel of accumulator chunk j
 #pragma unroll
     for (int j = 0; j < NC; ++j) coff[j] = 16u * (chunk0 + (uint32_t)((j + rot) & (NC - 1)));
-    const uint32_t sbase = smem_addr(smem);
     const int WWm = tg.WW - 1, WHm = tg.WH - 1;
 
 #pragma unroll(KP > 0 ? KP : 1)
@@ -172,17 +174,17 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
       if (ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm) {
         // the cell is in the window: corners from shared memory, zeros
         // standing for pixels outside the image
-        const uint32_t a00 = sbase + (uint32_t)(cy * tg.WW + cx) * rb;
-        const uint32_t at[4] = {a00, a00 + rb, a00 + (uint32_t)tg.WW * rb,
-                                a00 + (uint32_t)tg.WW * rb + rb};
+        const unsigned char* a00 = smem + (uint32_t)(cy * tg.WW + cx) * rb;
+        const uint32_t at[4] = {0u, rb, wrb, wrb + rb};  // the corners' offsets
         const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t v[NW];
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
-            // accumulator chunk j takes the slice's chunk (j + rot) mod NC
-            const uint4 c = lds128(at[k] + coff[j]);
+            // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
+            // plain loads, so that the compiler may fold constant offsets
+            const uint4 c = *reinterpret_cast<const uint4*>(a00 + coff[j] + at[k]);
             v[4 * j] = c.x;
             v[4 * j + 1] = c.y;
             v[4 * j + 2] = c.z;
@@ -270,10 +272,10 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
   constexpr int bytes = CPT * (int)sizeof(T);
   if constexpr (bytes >= 16 && bytes <= 64) {
     const size_t smem = tg.win_bytes + 16;  // the window, then the barrier
-    auto k9 = fwd_tile_kernel<T, CPT, 9>;
-    auto k8 = fwd_tile_kernel<T, CPT, 8>;
-    auto k0 = fwd_tile_kernel<T, CPT, 0>;
-    auto k = kp.P == 9 ? k9 : kp.P == 8 ? k8 : k0;
+    const bool r128 = (size_t)tg.GB * kp.gc * sizeof(T) == 128;
+    auto k = kp.P == 9 ? (r128 ? fwd_tile_kernel<T, CPT, 9, 128> : fwd_tile_kernel<T, CPT, 9, 0>)
+           : kp.P == 8 ? (r128 ? fwd_tile_kernel<T, CPT, 8, 128> : fwd_tile_kernel<T, CPT, 8, 0>)
+                       : (r128 ? fwd_tile_kernel<T, CPT, 0, 128> : fwd_tile_kernel<T, CPT, 0, 0>);
     if (smem > 48 * 1024) {
       cudaError_t e =
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
