@@ -56,11 +56,11 @@ FALLBACK_HBM_GBS = 6400.0
 # source voids the figure.
 TRAFFIC = {
     # profiles/launches_t_stage1_f16.md: fwd_tile_kernel, per launch
-    "fwd@t_stage1_f16": {"bytes": 69_102_581 + 774_689, "sha": "980bf0c14887"},
+    "fwd@t_stage1_f16": {"bytes": 69_105_096 + 907_019, "sha": "a932a371beef"},
     # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
     # call (the accumulator's memset is not a kernel and is not counted)
-    "bwd@t_stage1_f16": {"bytes": 169_852_694 + 44_502_840 + 51_389_473 + 104_225,
-                         "sha": "0f47884a8933"},
+    "bwd@t_stage1_f16": {"bytes": 169_776_028 + 44_537_455 + 51_390_642 + 108_277,
+                         "sha": "932930369705"},
 }
 
 
