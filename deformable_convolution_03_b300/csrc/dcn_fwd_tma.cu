@@ -152,6 +152,10 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
     for (int j = 0; j < NC; ++j) coff[j] = 16u * (chunk0 + (uint32_t)((j + rot) & (NC - 1)));
     const int WWm = tg.WW - 1, WHm = tg.WH - 1;
 
+    // points whose cell leaves the window (rare) are marked here and done
+    // after the loop, so that the unrolled loop holds only the shared-memory
+    // path
+    unsigned long long far = 0ull;
 #pragma unroll(KP > 0 ? KP : 1)
     for (int p = 0; p < P; ++p) {
       float m;
@@ -168,53 +172,67 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
       const float y = location(d.y, kp.tap_y[p], scale, ref_y);
       if (!in_box(x, y, kp.W, kp.H)) continue;  // also NaN / inf
       const float xf = floorf(x), yf = floorf(y);
+      const int cx = (int)xf - wx0, cy = (int)yf - wy0;
+      if (!(ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm)) {
+        far |= 1ull << p;
+        continue;
+      }
+      // the cell is in the window: corners from shared memory, zeros standing
+      // for pixels outside the image
+      const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
+      const float gym = gy * m, fym = fy * m;
+      const unsigned char* a00 = smem + (uint32_t)(cy * tg.WW + cx) * rb;
+      const uint32_t at[4] = {0u, rb, wrb, wrb + rb};  // the corners' offsets
+      const float w[4] = {gym * gx, gym * fx, fym * gx, fym * fx};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t v[NW];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
+          // plain loads, so that the compiler may fold constant offsets
+          const uint4 c = *reinterpret_cast<const uint4*>(a00 + coff[j] + at[k]);
+          v[4 * j] = c.x;
+          v[4 * j + 1] = c.y;
+          v[4 * j + 2] = c.z;
+          v[4 * j + 3] = c.w;
+        }
+        fma_words<T, NW>(acc, v, Fma<T>::weight(w[k]));
+      }
+    }
+    // far points: the point again, clamped corners from global memory,
+    // weight 0 outside the image
+    while (far) {
+      const int p = __ffsll((long long)far) - 1;
+      far &= far - 1;
+      float m = ld_once_1(mrow + p);
+      const float2 d = ld_once_2(orow + 2 * p);
+      if (kp.softmax) m = expf(m - mx) * inv;
+      const float x = location(d.x, kp.tap_x[p], scale, ref_x);
+      const float y = location(d.y, kp.tap_y[p], scale, ref_y);
+      const float xf = floorf(x), yf = floorf(y);
       const int x0 = (int)xf, y0 = (int)yf;
       const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
-      const int cx = x0 - wx0, cy = y0 - wy0;
-      if (ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm) {
-        // the cell is in the window: corners from shared memory, zeros
-        // standing for pixels outside the image
-        const unsigned char* a00 = smem + (uint32_t)(cy * tg.WW + cx) * rb;
-        const uint32_t at[4] = {0u, rb, wrb, wrb + rb};  // the corners' offsets
-        const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t v[NW];
-#pragma unroll
-          for (int j = 0; j < NC; ++j) {
-            // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
-            // plain loads, so that the compiler may fold constant offsets
-            const uint4 c = *reinterpret_cast<const uint4*>(a00 + coff[j] + at[k]);
-            v[4 * j] = c.x;
-            v[4 * j + 1] = c.y;
-            v[4 * j + 2] = c.z;
-            v[4 * j + 3] = c.w;
-          }
-          fma_words<T, NW>(acc, v, Fma<T>::weight(w[k]));
-        }
-      } else {
-        // far sample: clamped corners from global memory, weight 0 outside
-        const float wy0v = (uint32_t)y0 < H ? gy * m : 0.f;
-        const float wy1v = (uint32_t)(y0 + 1) < H ? fy * m : 0.f;
-        const float wx0v = (uint32_t)x0 < W ? gx : 0.f;
-        const float wx1v = (uint32_t)(x0 + 1) < W ? fx : 0.f;
-        const uint32_t xa = min((uint32_t)x0, W - 1), xb = min((uint32_t)(x0 + 1), W - 1);
-        const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
-        const uint32_t ra = ya * WC, rbb = yb * WC, ca = xa * C, cb = xb * C;
-        uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
-        ldg_words<NW>(img + (ra + ca), v00);
-        ldg_words<NW>(img + (ra + cb), v01);
-        ldg_words<NW>(img + (rbb + ca), v10);
-        ldg_words<NW>(img + (rbb + cb), v11);
-        rotate_chunks<NW>(v00, rot);
-        rotate_chunks<NW>(v01, rot);
-        rotate_chunks<NW>(v10, rot);
-        rotate_chunks<NW>(v11, rot);
-        fma_words<T, NW>(acc, v00, Fma<T>::weight(wy0v * wx0v));
-        fma_words<T, NW>(acc, v01, Fma<T>::weight(wy0v * wx1v));
-        fma_words<T, NW>(acc, v10, Fma<T>::weight(wy1v * wx0v));
-        fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1v * wx1v));
-      }
+      const float wy0v = (uint32_t)y0 < H ? gy * m : 0.f;
+      const float wy1v = (uint32_t)(y0 + 1) < H ? fy * m : 0.f;
+      const float wx0v = (uint32_t)x0 < W ? gx : 0.f;
+      const float wx1v = (uint32_t)(x0 + 1) < W ? fx : 0.f;
+      const uint32_t xa = min((uint32_t)x0, W - 1), xb = min((uint32_t)(x0 + 1), W - 1);
+      const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
+      const uint32_t ra = ya * WC, rbb = yb * WC, ca = xa * C, cb = xb * C;
+      uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
+      ldg_words<NW>(img + (ra + ca), v00);
+      ldg_words<NW>(img + (ra + cb), v01);
+      ldg_words<NW>(img + (rbb + ca), v10);
+      ldg_words<NW>(img + (rbb + cb), v11);
+      rotate_chunks<NW>(v00, rot);
+      rotate_chunks<NW>(v01, rot);
+      rotate_chunks<NW>(v10, rot);
+      rotate_chunks<NW>(v11, rot);
+      fma_words<T, NW>(acc, v00, Fma<T>::weight(wy0v * wx0v));
+      fma_words<T, NW>(acc, v01, Fma<T>::weight(wy0v * wx1v));
+      fma_words<T, NW>(acc, v10, Fma<T>::weight(wy1v * wx0v));
+      fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1v * wx1v));
     }
     unrotate_acc_t<CPT, T>(acc, rot);
     Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
