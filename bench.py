@@ -56,10 +56,10 @@ FALLBACK_HBM_GBS = 6400.0
 # source voids the figure.
 TRAFFIC = {
     # profiles/launches_t_stage1_f16.md: fwd_tile_kernel, per launch
-    "fwd@t_stage1_f16": {"bytes": 69_105_096 + 907_019, "sha": "a932a371beef"},
+    "fwd@t_stage1_f16": {"bytes": 69_082_635 + 850_042, "sha": "9a808e38e658"},
     # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
     # call (the accumulator's memset is not a kernel and is not counted)
-    "bwd@t_stage1_f16": {"bytes": 169_776_028 + 44_537_455 + 51_390_642 + 108_277,
+    "bwd@t_stage1_f16": {"bytes": 169_539_595 + 44_537_299 + 51_389_262 + 122_568,
                          "sha": "932930369705"},
 }
 
