@@ -204,7 +204,8 @@ void plan_fwd_tiles(const dcn_params_t* p, const Geometry& g, int cpt, dcn::KPar
 constexpr size_t kTileSmem = 64 * 1024;
 
 bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void* in,
-                   dcn::KParams* kp, dcn::TileGeom* tg, void* map, size_t budget = kTileSmem) {
+                   dcn::KParams* kp, dcn::TileGeom* tg, void* map, size_t budget = kTileSmem,
+                   bool any_shape = false) {
   if (!env_int("DCN_FWD_TMA", 1)) return false;
   const int es = elem_size(p->dtype);
   const long long C = (long long)p->G * p->gc;
@@ -221,21 +222,44 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
   const int per_px = GB * chunks;
   if (per_px > 256 || (per_px & (per_px - 1))) return false;
   const int px = 256 / per_px;
-  // least-padding power-of-two tile, then the squarest
   long long best = -1;
   int bw = 0, bh = 0;
-  for (int tw = 1; tw <= px; tw <<= 1) {
-    const int th = px / tw;
-    const long long padded = (long long)((g.Wo + tw - 1) / tw) * tw * ((g.Ho + th - 1) / th) * th;
-    const int skew = tw > th ? tw / th : th / tw;
-    const int bskew = bw > bh ? (bh ? bw / bh : 0) : (bw ? bh / bw : 0);
-    if (best < 0 || padded < best || (padded == best && skew < bskew)) {
-      best = padded;
-      bw = tw;
-      bh = th;
+  if (any_shape) {
+    // any tw x th tile whose block (tw * th * per_px threads, rounded up to
+    // whole warps) fits 256 threads: the fewest warps launched over the plane,
+    // then the fewest blocks, then the squarest.  Small planes (14 x 14, 7 x 7)
+    // take tiles such as 7 x 7 that no power-of-two shape matches.
+    long long bblocks = 0;
+    for (int tw = 1; tw <= px && tw <= g.Wo; ++tw)
+      for (int th = 1; tw * th <= px && th <= g.Ho; ++th) {
+        const long long blocks = (long long)((g.Wo + tw - 1) / tw) * ((g.Ho + th - 1) / th);
+        const long long warps = blocks * ((tw * th * per_px + 31) / 32);
+        const int skew = tw > th ? tw - th : th - tw, bskew = bw > bh ? bw - bh : bh - bw;
+        if (best < 0 || warps < best || (warps == best && blocks < bblocks) ||
+            (warps == best && blocks == bblocks && skew < bskew)) {
+          best = warps;
+          bblocks = blocks;
+          bw = tw;
+          bh = th;
+        }
+      }
+    // more than 20 % of the launched lanes idle
+    if (best * 32 * 5 > (long long)g.Wo * g.Ho * per_px * 6) return false;
+  } else {
+    // least-padding power-of-two tile of 256 threads, then the squarest
+    for (int tw = 1; tw <= px; tw <<= 1) {
+      const int th = px / tw;
+      const long long padded = (long long)((g.Wo + tw - 1) / tw) * tw * ((g.Ho + th - 1) / th) * th;
+      const int skew = tw > th ? tw / th : th / tw;
+      const int bskew = bw > bh ? (bh ? bw / bh : 0) : (bw ? bh / bw : 0);
+      if (best < 0 || padded < best || (padded == best && skew < bskew)) {
+        best = padded;
+        bw = tw;
+        bh = th;
+      }
     }
+    if (best * 5 > (long long)g.Wo * g.Ho * 6) return false;  // more than 20 % padding
   }
-  if (best * 5 > (long long)g.Wo * g.Ho * 6) return false;  // more than 20 % padding
   const double os = p->offset_scale;
   const int cw = p->dilation_w * (p->kernel_w - 1) / 2, ch = p->dilation_h * (p->kernel_h - 1) / 2;
   const double x0 = -cw * os, x1 = ((p->kernel_w - 1) * p->dilation_w - cw) * os;
@@ -493,7 +517,8 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   const int cpt = pick_fwd_cpt(p, g, input, output);
   alignas(64) unsigned char map[128];
   dcn::TileGeom tg;
-  const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map);
+  const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, kTileSmem,
+                                             env_int("DCN_FWD_ANY_TILE", 1) != 0);
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
   if (tile)

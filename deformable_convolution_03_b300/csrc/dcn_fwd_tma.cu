@@ -301,7 +301,11 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
     }
     const long long grid = (long long)kp.N * kp.tiles_w * kp.tiles_h * tg.ngb;
     if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-    k<<<(unsigned)grid, 256, smem, s>>>(map, kp, tg, i_, o_, m_, y_);
+    // one thread per (tile pixel, group of the block, channel slice), in whole
+    // warps: 256 for the power-of-two tiles, fewer for tiles such as 7 x 7
+    const int threads = (kp.tile_w * kp.tile_h * tg.GB * (kp.gc / CPT) + 31) / 32 * 32;
+    if (threads > 256) return cudaErrorInvalidConfiguration;
+    k<<<(unsigned)grid, threads, smem, s>>>(map, kp, tg, i_, o_, m_, y_);
     return cudaGetLastError();
   } else {
     return cudaErrorInvalidValue;
