@@ -56,10 +56,10 @@ FALLBACK_HBM_GBS = 6400.0
 # source voids the figure.
 TRAFFIC = {
     # profiles/launches_t_stage1_f16.md: fwd_tile_kernel, per launch
-    "fwd@t_stage1_f16": {"bytes": 69_082_635 + 850_042, "sha": "9a808e38e658"},
+    "fwd@t_stage1_f16": {"bytes": 69_082_390 + 851_812, "sha": "47abd65c757c"},
     # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
     # call (the accumulator's memset is not a kernel and is not counted)
-    "bwd@t_stage1_f16": {"bytes": 169_539_595 + 44_537_299 + 51_389_262 + 122_568,
+    "bwd@t_stage1_f16": {"bytes": 169_791_521 + 44_494_893 + 51_389_229 + 112_952,
                          "sha": "932930369705"},
 }
 
