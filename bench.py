@@ -10,7 +10,9 @@ storage), on seeded synthetic inputs already resident in HBM.
               all ranks (each rank runs its own batch: weak scaling)
   ideal     = every tensor the op reads or writes, counted once
   e2e       = the same metric with the inputs copied from pinned host memory
-              and every result copied back inside each timed step
+              and every result copied back inside each timed step, steps
+              streamed so that copies and compute overlap (the one-at-a-time
+              figure beside it as "serial")
   roofline  = the dominant phase (the backward call) against the measured HBM
               copy bandwidth; the forward kernel's own roofline beside it
   images/s  = FlashInternImage-T core-op throughput: 64 images over the sum of
@@ -212,23 +214,26 @@ class Case:
         self.ws_bytes = B.dcn_core_bwd_workspace(self.p)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
 
-    def fwd(self, x=None):
+    def fwd(self, x=None, res=None):
         x = x or self.x
+        out = (res or self.results())[0]
         if self.layout == "merged":
-            B.dcn_core_fwd_om(self.p, x["input"], x["offset_mask"], self.stride, self.out)
+            B.dcn_core_fwd_om(self.p, x["input"], x["offset_mask"], self.stride, out)
         else:
-            B.dcn_core_fwd(self.p, x["input"], x["offset"], x["mask"], self.out)
+            B.dcn_core_fwd(self.p, x["input"], x["offset"], x["mask"], out)
 
-    def bwd(self, x=None):
+    def bwd(self, x=None, res=None):
         x = x or self.x
+        r = res or self.results()
         if self.layout == "merged":
             B.dcn_core_bwd_om(self.p, x["grad_out"], x["input"], x["offset_mask"], self.stride,
-                              self.gi, self.go, self.ws, self.ws_bytes)
+                              r[1], r[2], self.ws, self.ws_bytes)
         else:
-            B.dcn_core_bwd(self.p, x["grad_out"], x["input"], x["offset"], x["mask"], self.gi,
-                           self.go, self.gm, self.ws, self.ws_bytes)
+            B.dcn_core_bwd(self.p, x["grad_out"], x["input"], x["offset"], x["mask"], r[1],
+                           r[2], r[3], self.ws, self.ws_bytes)
 
     def results(self):
+        """output, grad_input, grad_offset (or grad_offset_mask), grad_mask."""
         return [t for t in (self.out, self.gi, self.go, self.gm) if t is not None]
 
     def ideal(self) -> dict:
@@ -264,7 +269,8 @@ def timed_steps(case: Case, steps: int, flush: torch.Tensor, phases=("fwd", "bwd
 
 
 def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
-    """The step through host buffers: pinned inputs in, every result out."""
+    """The step through host buffers, one at a time: pinned inputs in, the
+    forward and backward, every result out, then the next step."""
     hin = {k: v.pin_memory() for k, v in case.host.items()}
     hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in case.results()]
     dev = {k: torch.empty_like(v) for k, v in case.x.items()}
@@ -286,6 +292,54 @@ def e2e_steps(case: Case, steps: int, flush: torch.Tensor):
         if k >= 2:
             times.append(a.elapsed_time(b))
     return times, h2d, d2h
+
+
+def e2e_pipelined(case: Case, steps: int, flush: torch.Tensor) -> float:
+    """The same steps streamed: every step still copies its inputs in from
+    pinned host memory and all its results out, but on three streams with two
+    device buffer sets, so that step k+1's inputs travel in and step k-1's
+    results travel out while step k computes (the host link's two directions
+    and the GPU work overlap).  L2 is flushed before each step's compute, on
+    the compute stream.  Returns ms per step over all steps (device events
+    from the first upload to the last download) and the last step's results
+    as they arrived in host memory."""
+    hin = {k: v.pin_memory() for k, v in case.host.items()}
+    bufs = [{k: torch.empty_like(v) for k, v in case.x.items()} for _ in range(2)]
+    res = [[torch.empty_like(t) for t in case.results()] for _ in range(2)]
+    hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in case.results()]
+            for _ in range(2)]
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    e_in = [ev() for _ in range(steps)]
+    e_c = [ev() for _ in range(steps)]
+    e_out = [ev() for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(s_in)
+    for k in range(steps):
+        j = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(e_c[k - 2])        # buffer set j's inputs are consumed
+            for key, d in bufs[j].items():
+                d.copy_(hin[key], non_blocking=True)
+            e_in[k].record(s_in)
+        with torch.cuda.stream(s_c):
+            s_c.wait_event(e_in[k])
+            if k >= 2:
+                s_c.wait_event(e_out[k - 2])       # result set j has been read out
+            flush.zero_()
+            case.fwd(bufs[j], res[j])
+            case.bwd(bufs[j], res[j])
+            e_c[k].record(s_c)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e_c[k])
+            for h, d in zip(hout[j], res[j]):
+                h.copy_(d, non_blocking=True)
+            e_out[k].record(s_out)
+    end.record(s_out)
+    end.synchronize()
+    return start.elapsed_time(end) / steps, hout[(steps - 1) % 2]
 
 
 def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
@@ -530,10 +584,19 @@ def main():
     e2e = None
     if args.e2e_steps > 0:
         e2e_t, h2d, d2h = e2e_steps(case, args.e2e_steps, flush)
-        e2e_ms = max_over_ranks([statistics.median(e2e_t)], dist, dev)[0]
-        e2e = {"value": round(aggregate_gbs(step_bytes, world, e2e_ms), 3), "unit": UNIT,
+        serial_ms = max_over_ranks([statistics.median(e2e_t)], dist, dev)[0]
+        e2e_pipelined(case, 3, flush)  # warm-up: streams, pinned buffers
+        pipe_ms = max_over_ranks([e2e_pipelined(case, args.e2e_steps, flush)[0]], dist, dev)[0]
+        e2e = {"value": round(aggregate_gbs(step_bytes, world, pipe_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e2e_ms, 4)}
+               "ms_per_step": round(pipe_ms, 4),
+               "how": "every step copies its inputs in from pinned host memory and every result "
+                      "out; steps streamed over three streams with two device buffer sets, so a "
+                      "step's compute overlaps the next step's upload and the previous step's "
+                      "download; L2 flushed before each step's compute",
+               "serial": {"value": round(aggregate_gbs(step_bytes, world, serial_ms), 3),
+                          "ms_per_step": round(serial_ms, 4),
+                          "how": "one step at a time: upload, compute, download, then the next"}}
 
     peak, peak_kind = hbm_peak()
     fwd_gbs = ib["fwd"] / (fwd_ms * 1e-3) / 1e9
