@@ -750,14 +750,14 @@ static bool encode_rows(CUtensorMap* m, int dtype, const void* base, long long r
 // Shared memory of the persistent kernel with S x stages and YB output
 // staging buffers (two if they fit, else one; 0 when not even S = 2, YB = 1
 // fits in 227 KB).
-static size_t linear_ws_smem(int K, int N, int* S_out, int* YB_out) {
+static size_t linear_ws_smem(int K, int N, int* S_out, int* YB_out, size_t budget = 227 * 1024) {
   const size_t KB = K / 64, w = KB * N * 128, a = KB * 128 * 128,
                y = (size_t)128 * ((N + 63) / 64) * 128,
                bars = 8 * (1 + 2 * 4 + 4) + 16 + 4 * (size_t)N;
   for (int YB = 2; YB >= 1; --YB)
     for (int S = 4; S >= 2; --S) {
       const size_t total = 1024 + w + S * a + YB * y + bars;
-      if (total <= 227 * 1024) {
+      if (total <= budget) {
         *S_out = S;
         *YB_out = YB;
         return total;
@@ -853,7 +853,14 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
       int tcols = 32;
       while (tcols < N) tcols <<= 1;
       int S = 0, YB = 0;
-      const size_t wsm = linear_ws_smem(K, N, &S, &YB);
+      // CTAs per SM: two when both fit (shared memory and 2 x 2 x tcols
+      // tensor-memory columns), so that one CTA's epilogue overlaps the other's
+      int per_sm = env_int_dev("DCN_LINEAR_CTAS", 2) >= 2 && 4 * tcols <= 512 ? 2 : 1;
+      size_t wsm = linear_ws_smem(K, N, &S, &YB, per_sm == 2 ? 113 * 1024 : 227 * 1024);
+      if (!wsm && per_sm == 2) {
+        per_sm = 1;
+        wsm = linear_ws_smem(K, N, &S, &YB);
+      }
       if (wsm && 2 * tcols <= 512 && N % 64 == 0 && env_int_dev("DCN_LINEAR_PERSIST", 1)) {
         cudaError_t e = cudaFuncSetAttribute(linear_ws_kernel<T>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm);
@@ -862,7 +869,7 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev_of_stream());
         if (e != cudaSuccess) return e;
         const int ntiles = (int)((M + 127) / 128);
-        const int grid = ntiles < sms ? ntiles : sms;
+        const int grid = ntiles < per_sm * sms ? ntiles : per_sm * sms;
         linear_ws_kernel<T><<<grid, 320, wsm, s>>>(xm, wm, ym, N, K / 64, tcols, S, YB, ntiles,
                                                    b_);
         return cudaGetLastError();
