@@ -143,6 +143,17 @@ def test_tma_forward_geometries(geom):
     check_fwd(w, make_inputs(w))
 
 
+@pytest.mark.parametrize("H,W", [(14, 14), (7, 7), (13, 9), (5, 30), (30, 5), (1, 40), (40, 1),
+                                 (3, 3)])
+@pytest.mark.parametrize("dt,gc,G", [("f16", 16, 4), ("bf16", 16, 16), ("bf16", 32, 2)])
+def test_tma_forward_plane_shapes(H, W, dt, gc, G):
+    # small and elongated planes, where the tile of fewest warps is not a
+    # power of two (7 x 7, 14 x 4, 1 x 40 ...) and blocks have fewer than 256
+    # threads
+    w = small(f"tmap_{dt}_{gc}_{G}_{H}x{W}", dt, gc=gc, G=G, N=3, H=H, W=W, offset_std=2.0)
+    check_fwd(w, make_inputs(w))
+
+
 SPLIT = [
     small("sp_f16_g16", "f16", gc=16, G=4, N=2, H=21, W=19),
     small("sp_f32_far", "f32", gc=16, G=2, N=2, H=20, W=23, offset_std=7.0),
