@@ -310,18 +310,28 @@ linear_ws_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     // ---- producer
     mbar_expect_tx(wfull, (uint32_t)(KB * N * 128));
     for (int kb = 0; kb < KB; ++kb) tma_load_2d(ws + kb * N * 128, &wmap, wfull, kb * 64, 0);
-    int i = 0;
+    int i = 0, last = -1;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
       const int st = i % S;
       if (!wait_or_abort(&aempty[st], ((i / S) & 1) ^ 1, abort)) break;
       mbar_expect_tx(&afull[st], (uint32_t)(KB * 128 * 128));
       for (int kb = 0; kb < KB; ++kb)
         tma_load_2d(as + (st * KB + kb) * 128 * 128, &xmap, &afull[st], kb * 64, t * 128);
+      last = i;
+    }
+    if (*abort) {
+      // leave no copy in flight into shared memory the next block may own:
+      // W, and the latest copy into each stage (earlier ones completed before
+      // their stage was refilled); every wait bounded
+      mbar_wait_bounded(wfull, 0, kLinearWaitPolls);
+      for (int j = last - S + 1 > 0 ? last - S + 1 : 0; j <= last; ++j)
+        mbar_wait_bounded(&afull[j % S], (uint32_t)((j / S) & 1), kLinearWaitPolls);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
     const uint32_t idesc = mma_idesc(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u,
                                      (uint32_t)N, 128u);
+    int last = -1;
     if (wait_or_abort(wfull, 0, abort)) {
       int i = 0;
       for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
@@ -351,8 +361,13 @@ linear_ws_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                 smem_addr(&tfull[b]))
             : "memory");
+        last = i;
       }
     }
+    // on abort, the MMAs already issued must finish before tensor memory is
+    // freed: the last commit tracks all of them (bounded)
+    if (*abort && last >= 0)
+      mbar_wait_bounded(&tfull[last & 1], (uint32_t)((last >> 1) & 1), kLinearWaitPolls);
   } else if (warp >= 2) {
     // ---- epilogue: warp w reads tensor-memory lanes 32 * (w % 4) ... for the
     // columns of half (w - 2) / 4

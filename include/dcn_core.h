@@ -161,16 +161,24 @@ int dcn_core_bwd_om(const dcn_params_t* p, const void* grad_out, const void* inp
  * float16 / bfloat16.  This entry point computes exactly what dcn_core_bwd
  * computes, with the same arguments minus the workspace, and takes its
  * float32 accumulator from a static array inside the library
- * (DCN_NOALLOC_SCRATCH_BYTES per GPU that loads the library, held until the
- * process exits).  It allocates nothing and calls no allocating routine.
+ * (DCN_NOALLOC_SCRATCH_BYTES on each GPU where the library's module is
+ * loaded, held until the process exits).  The call itself allocates nothing
+ * and calls no allocating routine.
  *
  *   - Requests whose dcn_core_bwd_workspace(p) exceeds
  *     DCN_NOALLOC_SCRATCH_BYTES return DCN_ERR_UNSUPPORTED before any CUDA
  *     call; other argument errors are those of dcn_core_bwd.
  *   - The first call on a device (that needs the array: float16 / bfloat16)
- *     looks up the array's device address on the current device, once; make
- *     that first call before any stream capture.  The stream must belong to
- *     the current device.
+ *     looks up the array's device address on the current device, once.  The
+ *     array is reserved when the CUDA module holding it is loaded on that
+ *     device: with CUDA's default lazy module loading that happens at this
+ *     first lookup, so a runtime that hands out all device memory later
+ *     should make the first call at start-up (or set
+ *     CUDA_MODULE_LOADING=EAGER, which reserves it when the context is
+ *     created).  Make that first call before any stream capture.  The stream
+ *     must belong to the current device.  cudaDeviceReset invalidates the
+ *     remembered address: do not call this entry point on a device after
+ *     resetting it.
  *   - All calls on a device share the one array.  Each call clears what it
  *     uses before use, but two calls whose work overlaps on the GPU (different
  *     streams, no ordering between them) race on it and give wrong results:

@@ -20,6 +20,12 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # fails validation, or stops at the fault hook before any CUDA call)
 A = 1 << 20
 
+# Tests that hand the library fake device addresses run only where no GPU
+# exists: should a check ever regress and let such a call through, it then
+# fails at the launch instead of touching a shared device's memory.
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake pointers only where no GPU exists")
+
 
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "dcn_core.h")).read()
@@ -84,6 +90,7 @@ BAD = [
 ]
 
 
+@host_only
 @pytest.mark.parametrize("bad,code", BAD)
 def test_invalid_parameters_rejected_by_every_entry(native, bad, code):
     p = native.Params(**{**dict(N=1, H=8, W=8, G=2, gc=4), **bad})
@@ -98,6 +105,7 @@ def test_invalid_parameters_rejected_by_every_entry(native, bad, code):
     assert code in native.dcn_status_str(want)
 
 
+@host_only
 def test_null_arguments(native):
     lib = native.lib()
     p = native.Params(N=1, H=8, W=8, G=2, gc=4)
@@ -114,6 +122,7 @@ def test_null_arguments(native):
         assert lib.dcn_core_bwd(ctypes.byref(p.c()), *ptrs, None, 0, None) == native.DCN_ERR_NULL
 
 
+@host_only
 def test_misaligned_pointers(native):
     lib = native.lib()
     for dtype, es in ((native.DCN_F32, 4), (native.DCN_F16, 2), (native.DCN_BF16, 2)):
@@ -132,6 +141,7 @@ def test_misaligned_pointers(native):
                                     None) == native.DCN_ERR_ALIGN
 
 
+@host_only
 def test_workspace_checks(native):
     lib = native.lib()
     p = native.Params(N=2, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)
@@ -150,7 +160,7 @@ def test_empty_batch_is_a_no_op(native):
     assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([None] * 8), 0, None) == native.DCN_OK
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers only where no GPU exists")
+@host_only
 def test_fault_hook_reports_cuda_error(native, monkeypatch):
     lib = native.lib()
     p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)
@@ -167,6 +177,7 @@ def test_status_strings(native):
     assert "unknown" in native.dcn_status_str(99)
 
 
+@host_only
 def test_merged_layout_argument_checks(native):
     lib = native.lib()
     p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)   # P = 9
@@ -189,6 +200,7 @@ def _lin(native, M, K, N, dtype=None):
     return native.dcn_linear_params_t(M, K, N, native.DCN_F16 if dtype is None else dtype)
 
 
+@host_only
 def test_linear_argument_errors(native):
     import ctypes
     L = native.lib()
@@ -215,6 +227,7 @@ def _cfs(native, M, C, G, dtype=None):
     return native.dcn_cfs_params_t(M, C, G, native.DCN_F16 if dtype is None else dtype)
 
 
+@host_only
 def test_centre_feature_scale_argument_errors(native):
     import ctypes
     L = native.lib()

@@ -51,11 +51,25 @@ def test_config_backward_full_size(name):
     check_bwd(w, make_inputs(w))
 
 
-@pytest.mark.parametrize("name", ["t_stage1_f16", "t_stage2_bf16", "g_stage1_rc_bf16"])
-def test_config_backward_16bit(name):
-    # backward of the 16-bit workloads (two images, to keep the oracle quick)
-    w = WORKLOADS[name].with_(N=2, backward=True)
+BWD16 = CONFIGS[2] + CONFIGS[3] + CONFIGS[4]
+
+
+@pytest.mark.parametrize("name", BWD16)
+def test_config_backward_16bit_full_size(name):
+    # the 16-bit backward at the full size the benchmark times (64 images at
+    # the FlashInternImage-T stages, InternImage-G stage 1 with and without
+    # its centre tap), every element against the oracle
+    w = WORKLOADS[name].with_(backward=True)
     check_bwd(w, make_inputs(w, grad=True))
+
+
+@pytest.mark.parametrize("name", BWD16)
+def test_config_forward_against_binary64_locations(name):
+    # the oracle with its sampling locations in binary64 throughout (no shared
+    # binary32 rounding before floor): the forward is continuous across cell
+    # edges, so it must meet the same tolerance
+    w = WORKLOADS[name]
+    check_fwd(w, make_inputs(w), coord_f32=0)
 
 
 # ---- small ragged cases --------------------------------------------------------

@@ -4,10 +4,11 @@ Some callers may not allocate device memory where they run the backward (a
 plugin inside a runtime that owns all device memory, or code with a fixed
 memory budget), so they cannot hand dcn_core_bwd the float32 workspace that
 float16 / bfloat16 need.  dcn_core_bwd_noalloc takes that accumulator from a
-static array inside the library instead.  These tests check that it gives
-what dcn_core_bwd gives, on two calls in a row (the array keeps the previous
-call's contents, which must not leak into the next result), and that requests
-larger than the array are refused before any CUDA call.
+static array inside the library instead.  These tests check its results
+against the oracle and against dcn_core_bwd, on two calls in a row (the array
+keeps the previous call's contents, which must not leak into the next
+result), and that requests larger than the array are refused before any
+CUDA call.
 
 This file is collected last on purpose.
 """
@@ -19,7 +20,8 @@ import torch
 from deformable_convolution_03_b300 import binding as B
 from deformable_convolution_03_b300.inputs import WORKLOADS, make_inputs
 
-from parity import assert_close, lib_params
+import oracle
+from parity import assert_close, f64, lib_params, oracle_params
 
 
 def _backward(w, t, noalloc: bool):
@@ -41,9 +43,9 @@ def _backward(w, t, noalloc: bool):
 
 
 @pytest.mark.gpu
-@pytest.mark.usefixtures("native")
+@pytest.mark.usefixtures("native", "oracle_lib")
 @pytest.mark.parametrize("name", ["t_stage1_f16", "g_stage1_rc_bf16", "fb28_f32"])
-def test_noalloc_backward_matches_workspace_backward(name):
+def test_noalloc_backward_matches_oracle_and_workspace_backward(name):
     base = WORKLOADS[name]
     w = base.with_(N=8 if base.N > 8 else base.N, backward=True)
     if base.name.startswith("g_stage1"):
@@ -53,21 +55,25 @@ def test_noalloc_backward_matches_workspace_backward(name):
         t = make_inputs(w, seed=seed, grad=True)
         want = _backward(w, t, noalloc=False)
         got = _backward(w, t, noalloc=True)
-        for name_, a, b in zip(("grad_input", "grad_offset", "grad_mask"), got, want):
-            ref = b.detach().to("cpu", torch.float64).numpy()
-            assert_close(a, ref, w.dtype, f"call {call}: {name_}")
+        ref = oracle.backward(oracle_params(w), f64(t["grad_out"]), f64(t["input"]),
+                              f64(t["offset"]), f64(t["mask"]))
+        for name_, a, b, r in zip(("grad_input", "grad_offset", "grad_mask"), got, want, ref):
+            assert_close(a, r, w.dtype, f"call {call}: {name_} against the oracle")
+            assert_close(a, f64(b), w.dtype, f"call {call}: {name_} against dcn_core_bwd")
 
 
 @pytest.mark.usefixtures("native")
 def test_noalloc_refuses_requests_beyond_the_scratch():
     # 64 images of 56x56x64 need 51 MB of accumulator: refused before any CUDA
-    # call, so the (never dereferenced) fake addresses below are safe
+    # call.  The tensors are NULL: the size check comes before the pointer
+    # check, and a call that got past it would stop at DCN_ERR_NULL, never
+    # at a launch.
     w = WORKLOADS["t_stage1_f16"]
     p = lib_params(w)
     assert B.dcn_core_bwd_workspace(p) > B.DCN_NOALLOC_SCRATCH_BYTES
-    a = 1 << 20
-    rc = B.lib().dcn_core_bwd_noalloc(ctypes.byref(p.c()), a, a, a, a, a, a, a, None)
+    rc = B.lib().dcn_core_bwd_noalloc(ctypes.byref(p.c()), None, None, None, None, None, None,
+                                      None, None)
     assert rc == B.DCN_ERR_UNSUPPORTED
     bad = lib_params(w.with_(N=-1))
-    assert B.lib().dcn_core_bwd_noalloc(ctypes.byref(bad.c()), a, a, a, a, a, a, a,
-                                        None) == B.DCN_ERR_SHAPE
+    assert B.lib().dcn_core_bwd_noalloc(ctypes.byref(bad.c()), None, None, None, None, None,
+                                        None, None, None) == B.DCN_ERR_SHAPE
