@@ -13,6 +13,7 @@
 
 #include "../../include/dcn_core.h"
 #include "dcn_kernels.h"
+#include "dcn_options.h"
 
 namespace {
 
@@ -114,30 +115,21 @@ void fill_kparams(const dcn_params_t* p, const Geometry& g, dcn::KParams* kp) {
     }
 }
 
-// Host-side fault hook for tests of the error path: with DCN_FAULT_INJECT=launch
-// in the environment a valid call reports DCN_ERR_CUDA instead of launching.
-bool fault_injected() {
-  const char* v = std::getenv("DCN_FAULT_INJECT");
-  return v && std::strcmp(v, "launch") == 0;
-}
-
-int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  if (!v || !*v) return dflt;
-  return std::atoi(v);
-}
+// Host-side fault hook for tests of the error path: with the fault_inject
+// switch set, a valid call reports DCN_ERR_CUDA instead of launching.
+bool fault_injected() { return dcn::options().fault_inject != 0; }
 
 // Channels per thread of the forward.  The wide kernel (returned negated)
 // takes slices of 16 channels (or 8, 4) of 16 to 64 bytes when the unit count
 // and every image's element count fit in 31 bits and the input and output are
 // 32-byte aligned (16 for a 16-byte slice).  Otherwise the general kernel with
 // the widest power of two dividing gc up to one 16-byte vector (or
-// DCN_FWD_CPT), whose slices start aligned in both the input and the output.
+// the fwd_cpt switch), whose slices start aligned in both the input and the output.
 int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const void* out) {
   const int es = elem_size(p->dtype);
   const long long img = (long long)p->H * p->W * p->G * p->gc;
-  if (env_int("DCN_FWD_WIDE", 1) && img < (1LL << 31)) {
-    const int wcap = env_int("DCN_FWD_WIDE_CPT", 16);
+  if (dcn::options().fwd_wide && img < (1LL << 31)) {
+    const int wcap = dcn::options().fwd_wide_cpt;
     for (int c = 16; c >= 4; c >>= 1) {
       if (c > wcap) continue;
       const int bytes = c * es;
@@ -147,7 +139,7 @@ int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const
       if (aligned(in, a) && aligned(out, a)) return -c;
     }
   }
-  int cap = env_int("DCN_FWD_CPT", 16 / es);
+  int cap = (dcn::options().fwd_cpt > 0 ? dcn::options().fwd_cpt : 16 / es);
   for (int c = 32; c >= 1; c >>= 1) {
     if (c > cap || p->gc % c) continue;
     const size_t a = (size_t)(c * es < 16 ? c * es : 16);
@@ -161,13 +153,13 @@ int pick_fwd_cpt(const dcn_params_t* p, const Geometry& g, const void* in, const
 // = px, the one that pads the output plane least (then the squarest) is
 // taken, and only when the padding wastes at most 20 % of the threads;
 // otherwise (and when G times the slices per unit is not a power of two up to
-// 256, or with DCN_FWD_TILE=0) blocks take consecutive items.  Measured on
+// 256, or with the fwd_tile switch off) blocks take consecutive items.  Measured on
 // B300: FlashInternImage-T stage 1 (56^2, 8x8 tiles) 79.9 -> 73.7 us,
 // 64 x 28^2 x 128 fp32 131 -> 117 us, from better L1 reuse of the input;
 // shapes that padded 7x7 or 13x13 planes by a third were slower.
 void plan_fwd_tiles(const dcn_params_t* p, const Geometry& g, int cpt, dcn::KParams* kp) {
   kp->tile_w = kp->tile_h = kp->tiles_w = kp->tiles_h = 0;
-  if (!env_int("DCN_FWD_TILE", 1)) return;
+  if (!dcn::options().fwd_tile) return;
   const long long per_px = (long long)p->G * (p->gc / cpt);
   if (per_px > 256 || (per_px & (per_px - 1))) return;
   const int px = (int)(256 / per_px);
@@ -197,16 +189,16 @@ void plan_fwd_tiles(const dcn_params_t* p, const Geometry& g, int cpt, dcn::KPar
 // (all of them when a pixel's channels fit in 128 bytes, else the largest
 // divisor of G that does), a power-of-two tile of 256 / (GB * gc/cpt) output
 // pixels, and a window of the tile's footprint plus a halo of R pixels, R from
-// 6 (DCN_FWD_HALO) down to 0 so that the window stays within kTileSmem (three
+// 6 (the fwd_halo switch) down to 0 so that the window stays within kTileSmem (three
 // blocks per SM).  Needs the input 16-byte aligned and every tensor-map
-// stride a multiple of 16 bytes; fills the tensor map.  DCN_FWD_TMA=0 turns it
+// stride a multiple of 16 bytes; fills the tensor map.  The fwd_tma switch at 0 turns it
 // off.
 constexpr size_t kTileSmem = 64 * 1024;
 
 bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void* in,
                    dcn::KParams* kp, dcn::TileGeom* tg, void* map, size_t budget = kTileSmem,
                    bool any_shape = false) {
-  if (!env_int("DCN_FWD_TMA", 1)) return false;
+  if (!dcn::options().fwd_tma) return false;
   const int es = elem_size(p->dtype);
   const long long C = (long long)p->G * p->gc;
   if (!aligned(in, 16) || (C * es) % 16 || (p->gc * es) % 16) return false;
@@ -267,7 +259,7 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
   const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
   const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
   const size_t rb = (size_t)GB * p->gc * es;
-  for (int R = env_int("DCN_FWD_HALO", 6); R >= 0; --R) {
+  for (int R = dcn::options().fwd_halo; R >= 0; --R) {
     const long long WH = (long long)(bh - 1) * p->stride_h + (tmax_y - tmin_y) + 2 + 2 * R;
     const long long WW = (long long)(bw - 1) * p->stride_w + (tmax_x - tmin_x) + 2 + 2 * R;
     if (WH > 256 || WW > 256 || (size_t)(WH * WW) * rb > budget) continue;
@@ -290,14 +282,14 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
 }
 
 // Channels per thread of the backward: a power of two dividing gc, at most 4
-// (or DCN_BWD_CPT), with gc/c a power of two no larger than 32 so that a
+// (or the bwd_cpt switch), with gc/c a power of two no larger than 32 so that a
 // unit's threads are adjacent lanes of one warp; 0 selects the kernel that
 // takes any gc.  Four float32 channels per lane make the lanes of one unit
 // cover whole 32-byte sectors of grad_input in a single vector reduction,
 // which halves the L2 reduction requests against one lane per 16 channels.
 int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const void* acc) {
   const int es = elem_size(p->dtype);
-  int cap = env_int("DCN_BWD_CPT", 4);
+  int cap = dcn::options().bwd_cpt;
   for (int c = 32; c >= 1; c >>= 1) {
     if (c > cap || p->gc % c) continue;
     const int chunks = p->gc / c;
@@ -321,13 +313,13 @@ int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const 
 // 2 / dilation 2 (64 x 28^2 x 128, fp32) it takes 68 us against 170 us for the
 // single-pass kernel; at stride 1 the window's shared memory takes L1
 // capacity away from the corner gathers and it is slower (FlashInternImage-T
-// stage 1: 588 us against 430 us).  DCN_BWD_WINDOW=1 uses it for every
+// stage 1: 588 us against 430 us).  The bwd_window switch at 1 uses it for every
 // geometry it can take, 0 never.
 constexpr size_t kWindowSmem = 64 * 1024;
 
 int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const void* gout,
                 const void* acc, dcn::WinGeom* wg) {
-  const int mode = env_int("DCN_BWD_WINDOW", 2);
+  const int mode = dcn::options().bwd_window;
   if (mode == 0) return 0;
   if (mode != 1 && p->stride_h < 2 && p->stride_w < 2) return 0;
   const int es = elem_size(p->dtype);
@@ -353,7 +345,7 @@ int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const 
   const double y0 = -ch * os, y1 = ((p->kernel_h - 1) * p->dilation_h - ch) * os;
   const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
   const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
-  for (int R = env_int("DCN_BWD_HALO", 6); R >= 1; --R) {
+  for (int R = dcn::options().bwd_halo; R >= 1; --R) {
     wg->TH = TH;
     wg->TW = TW;
     wg->WH = (TH - 1) * p->stride_h + (tmax_y - tmin_y) + 2 * R + 2;
@@ -375,7 +367,7 @@ int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const 
 // over windows, one thread per output pixel of a TH x TW <= 256 tile of one
 // (image, group).  Of the tile shapes, the one with the least work (tiles x
 // (256 threads + window pixels)) is taken; the window is the tile's footprint
-// plus a halo of R pixels for the offsets, R from 6 (DCN_BWD_HALO) down to 1
+// plus a halo of R pixels for the offsets, R from 6 (the bwd_halo switch) down to 1
 // so that the shared memory stays within kSplitSmem (four CTAs per SM).
 // Needs gc*es of 16, 32 or 64 bytes, P <= 16, grad_out 32-byte aligned (16 for
 // 16-byte rows) and the float32 accumulator 16-byte aligned.  Returns the
@@ -386,7 +378,7 @@ int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const 
 // single-pass kernel; InternImage-G stage 1, bf16: 391 us against 539 us for
 // the fused window kernel).  For float32 the corner gathers of the sample
 // kernel cost twice as much and the single-pass or window kernels win
-// (64 x 28^2 x 128: 348 us against 227 us).  DCN_BWD_SPLIT=1 uses it for every
+// (64 x 28^2 x 128: 348 us against 227 us).  The bwd_split switch at 1 uses it for every
 // dtype it can take, 0 never.
 constexpr size_t kSplitSmem = 56 * 1024;
 constexpr size_t kStageSmem = 32 * 1024;
@@ -395,7 +387,7 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
                const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb,
                dcn::TileGeom* tg, void* map, bool* tma) {
   *tma = false;
-  const int mode = env_int("DCN_BWD_SPLIT", 2);
+  const int mode = dcn::options().bwd_split;
   if (mode == 0 || (mode != 1 && p->dtype == DCN_F32)) return 0;
   const int es = elem_size(p->dtype);
   const int row = p->gc * es;
@@ -414,7 +406,7 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
   const double y0 = -ch * os, y1 = ((p->kernel_h - 1) * p->dilation_h - ch) * os;
   const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
   const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
-  const int R0 = env_int("DCN_BWD_HALO", 6);
+  const int R0 = dcn::options().bwd_halo;
   long long best = -1;
   for (int TW = 1; TW <= 256 && TW <= g.Wo; ++TW) {
     const int TH = std::min(g.Ho, 256 / TW);
@@ -439,13 +431,13 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
   }
   if (best < 0 || (long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
   // the sample blocks read their corners through L1 over the wide forward's
-  // tiles.  DCN_BWD_TMA=1 stages their input windows by a tensor copy instead
-  // (the forward's TMA plan, windows within DCN_BWD_TMA_KB KB): measured
+  // tiles.  The bwd_tma switch stages their input windows by a tensor copy
+  // instead (the forward's TMA plan, windows within bwd_tma_kb KB): measured
   // slower inside the fused launch (FlashInternImage-T stage 1: 315-326 us
   // against 272 us), whose input blocks then get less L1.
-  const bool fused = env_int("DCN_BWD_FUSE", 1) != 0;
-  const size_t tma_budget = (size_t)env_int("DCN_BWD_TMA_KB", 40) * 1024;
-  if (fused && env_int("DCN_BWD_TMA", 0) && plan_fwd_tile(p, g, cpt, in, kp, tg, map, tma_budget))
+  const bool fused = dcn::options().bwd_fuse != 0;
+  const size_t tma_budget = (size_t)dcn::options().bwd_tma_kb * 1024;
+  if (fused && dcn::options().bwd_tma && plan_fwd_tile(p, g, cpt, in, kp, tg, map, tma_budget))
     *tma = true;
   else
     plan_fwd_tiles(p, g, cpt, kp);
@@ -458,7 +450,7 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     *la = 2 * g.P;
     *lb = g.P;
   }
-  if (!env_int("DCN_BWD_STAGE", 1) || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
+  if (!dcn::options().bwd_stage || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
   // staged rows are copied out per tile row, which needs every group of a
   // pixel in the block
   if (*tma && tg->GB != p->G) *la = *lb = 0;
@@ -512,13 +504,13 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
     kp.os_off = kp.os_mask = row_stride;
     kp.merged = 1;
     kp.merged_rows64 = g.P == 9 && es == 2 && aligned(offset, 32) &&
-                       (row_stride * es) % 32 == 0 && env_int("DCN_FWD_ROW64", 1);
+                       (row_stride * es) % 32 == 0 && dcn::options().fwd_row64;
   }
   const int cpt = pick_fwd_cpt(p, g, input, output);
   alignas(64) unsigned char map[128];
   dcn::TileGeom tg;
   const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, kTileSmem,
-                                             env_int("DCN_FWD_ANY_TILE", 1) != 0);
+                                             dcn::options().fwd_any_tile != 0);
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
   if (tile)
@@ -706,7 +698,7 @@ int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const
   if (!x || !w || !y) return DCN_ERR_NULL;
   if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || (bias && !aligned(bias, es)))
     return DCN_ERR_ALIGN;
-  const bool tc = env_int("DCN_LINEAR_TC", 1) && dcn::linear_tc_ok(p->dtype, p->M, p->K, p->N,
+  const bool tc = dcn::options().linear_tc && dcn::linear_tc_ok(p->dtype, p->M, p->K, p->N,
                                                                    x, w, y);
   if (fault_injected()) return DCN_ERR_CUDA;
   return cuda_status(dcn::launch_linear(p->dtype, p->M, p->K, p->N, x, w, bias, y, tc,
@@ -749,3 +741,59 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
 }
 
 }  // extern "C"
+
+// ---- the selection switches and their test hook ----------------------------
+
+namespace dcn {
+namespace {
+Options g_options;
+}
+const Options& options() { return g_options; }
+}  // namespace dcn
+
+namespace {
+struct OptionName {
+  const char* name;
+  int dcn::Options::*field;
+};
+constexpr OptionName kOptionNames[] = {
+    {"fwd_wide", &dcn::Options::fwd_wide},
+    {"fwd_wide_cpt", &dcn::Options::fwd_wide_cpt},
+    {"fwd_cpt", &dcn::Options::fwd_cpt},
+    {"fwd_tile", &dcn::Options::fwd_tile},
+    {"fwd_tma", &dcn::Options::fwd_tma},
+    {"fwd_halo", &dcn::Options::fwd_halo},
+    {"fwd_any_tile", &dcn::Options::fwd_any_tile},
+    {"fwd_row64", &dcn::Options::fwd_row64},
+    {"bwd_split", &dcn::Options::bwd_split},
+    {"bwd_fuse", &dcn::Options::bwd_fuse},
+    {"bwd_tma", &dcn::Options::bwd_tma},
+    {"bwd_tma_kb", &dcn::Options::bwd_tma_kb},
+    {"bwd_window", &dcn::Options::bwd_window},
+    {"bwd_cpt", &dcn::Options::bwd_cpt},
+    {"bwd_halo", &dcn::Options::bwd_halo},
+    {"bwd_stage", &dcn::Options::bwd_stage},
+    {"linear_tc", &dcn::Options::linear_tc},
+    {"linear_bn", &dcn::Options::linear_bn},
+    {"linear_yb", &dcn::Options::linear_yb},
+    {"linear_s", &dcn::Options::linear_s},
+    {"linear_ctas", &dcn::Options::linear_ctas},
+    {"linear_persist", &dcn::Options::linear_persist},
+    {"fault_inject", &dcn::Options::fault_inject},
+};
+}  // namespace
+
+// Test hooks, exported but not part of the public header: set one selection
+// switch by name (DCN_ERR_SHAPE for an unknown name), or put all of them back
+// to their defaults.  Not for concurrent use with calls on other threads.
+extern "C" int dcn_internal_set_option(const char* name, int value) {
+  if (!name) return DCN_ERR_NULL;
+  for (const OptionName& o : kOptionNames)
+    if (std::strcmp(o.name, name) == 0) {
+      dcn::g_options.*o.field = value;
+      return DCN_OK;
+    }
+  return DCN_ERR_SHAPE;
+}
+
+extern "C" void dcn_internal_reset_options(void) { dcn::g_options = dcn::Options(); }

@@ -23,6 +23,7 @@
 
 #include "dcn_common.cuh"
 #include "dcn_kernels.h"
+#include "dcn_options.h"
 
 namespace dcn {
 
@@ -327,11 +328,8 @@ round_kernel(const float* __restrict__ acc, T* __restrict__ out, long long n) {
   for (; i < n; i += stride) out[i] = Dt<T>::from_f(acc[i]);
 }
 
-// DCN_BWD_STAGE=0 writes grad_offset / grad_mask directly (for comparison).
-static int env_stage() {
-  const char* v = std::getenv("DCN_BWD_STAGE");
-  return !(v && v[0] == '0');
-}
+// the bwd_stage switch at 0 writes grad_offset / grad_mask directly
+static int env_stage() { return options().bwd_stage != 0; }
 
 template <typename T>
 static cudaError_t launch_bwd_t(const KParams& kp, int cpt, const void* gout, const void* in,

@@ -39,28 +39,9 @@
 
 #include "dcn_common.cuh"
 #include "dcn_kernels.h"
+#include "dcn_options.h"
 
 namespace dcn {
-
-// Copy `bytes` (even) from shared to global memory with the lanes of one warp,
-// in 16-byte pieces when both ends and the length allow it.
-__device__ __forceinline__ void warp_copy_out(void* dst, const void* src, int bytes, int lane) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
-                      static_cast<uintptr_t>(bytes);
-  if ((a & 15) == 0) {
-    uint4* d = static_cast<uint4*>(dst);
-    const uint4* s = static_cast<const uint4*>(src);
-    for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
-  } else if ((a & 3) == 0) {
-    uint32_t* d = static_cast<uint32_t*>(dst);
-    const uint32_t* s = static_cast<const uint32_t*>(src);
-    for (int i = lane; i < bytes / 4; i += 32) d[i] = s[i];
-  } else {
-    unsigned short* d = static_cast<unsigned short*>(dst);
-    const unsigned short* s = static_cast<const unsigned short*>(src);
-    for (int i = lane; i < bytes / 2; i += 32) d[i] = s[i];
-  }
-}
 
 // ---- the sample half --------------------------------------------------------
 // One thread per (unit, slice of CPT channels), slices of 16 to 64 bytes, in
@@ -988,7 +969,7 @@ static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T*
   return cudaGetLastError();
 }
 
-// Both halves as one launch of bwd_both_kernel (DCN_BWD_FUSE=0: two launches).
+// Both halves as one launch of bwd_both_kernel (the bwd_fuse switch at 0: two launches).
 template <typename T, int CPT, int NW>
 static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* go_, const T* i_,
                                  const T* o_, const T* m_, T* goff_, T* gm_, int la, int lb,
@@ -1037,8 +1018,7 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
   T* gm_ = static_cast<T*>(gmask);
   cudaError_t e;
   const int nw = kp.gc * (int)sizeof(T) / 4;
-  const char* fuse = std::getenv("DCN_BWD_FUSE");
-  if (!(fuse && fuse[0] == '0')) {
+  if (options().bwd_fuse) {
     // the (channels per sample thread, words per unit row) pairs that occur
     if constexpr (sizeof(T) == 2) {
       if (cpt == 8 && nw == 4)

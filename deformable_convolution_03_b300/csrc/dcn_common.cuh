@@ -187,6 +187,7 @@ template <> struct Dt<__half> {
     return __half22float2(__ldg(reinterpret_cast<const __half2*>(p)));
   }
   __device__ __forceinline__ static __half from_f(float v) { return __float2half_rn(v); }
+  __device__ __forceinline__ static float to_f(__half v) { return __half2float(v); }
 };
 
 template <> struct Dt<__nv_bfloat16> {
@@ -206,6 +207,7 @@ template <> struct Dt<__nv_bfloat16> {
     return __bfloat1622float2(__ldg(reinterpret_cast<const __nv_bfloat162*>(p)));
   }
   __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+  __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 };
 
 // Loads of data read once (offsets, masks): not kept in L1, so that they do
@@ -493,6 +495,26 @@ __device__ __forceinline__ void fma_words(float* acc, const uint32_t (&v)[NW], t
   } else {
 #pragma unroll
     for (int i = 0; i < NW; i += 2) Fma<T>::pair(acc[i], acc[i + 1], v[i], v[i + 1], w);
+  }
+}
+
+// Copy `bytes` (even) from shared to global memory with the lanes of one warp,
+// in 16-byte pieces when both ends and the length allow it.
+__device__ __forceinline__ void warp_copy_out(void* dst, const void* src, int bytes, int lane) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
+                      static_cast<uintptr_t>(bytes);
+  if ((a & 15) == 0) {
+    uint4* d = static_cast<uint4*>(dst);
+    const uint4* s = static_cast<const uint4*>(src);
+    for (int i = lane; i < bytes / 16; i += 32) d[i] = s[i];
+  } else if ((a & 3) == 0) {
+    uint32_t* d = static_cast<uint32_t*>(dst);
+    const uint32_t* s = static_cast<const uint32_t*>(src);
+    for (int i = lane; i < bytes / 4; i += 32) d[i] = s[i];
+  } else {
+    unsigned short* d = static_cast<unsigned short*>(dst);
+    const unsigned short* s = static_cast<const unsigned short*>(src);
+    for (int i = lane; i < bytes / 2; i += 32) d[i] = s[i];
   }
 }
 

@@ -30,6 +30,7 @@
 
 #include "dcn_common.cuh"
 #include "dcn_kernels.h"
+#include "dcn_options.h"
 
 namespace dcn {
 
@@ -721,11 +722,6 @@ linear_simt_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
 
 // ---- host side ------------------------------------------------------------------
 
-static int env_int_dev(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  return v && *v ? std::atoi(v) : dflt;
-}
-
 static int dev_of_stream() {
   int d = 0;
   cudaGetDevice(&d);
@@ -782,9 +778,9 @@ static size_t linear_ws_smem(int K, int N, int* S_out, int* YB_out, size_t budge
 }
 
 // The K-loop kernel's output tile width: 256, 128 or 64 columns dividing N
-// (DCN_LINEAR_BN caps it).
+// (the linear_bn switch caps it).
 static int linear_kloop_bn(int N) {
-  const int cap = env_int_dev("DCN_LINEAR_BN", 256);
+  const int cap = options().linear_bn;
   for (int bn = 256; bn >= 64; bn >>= 1)
     if (bn <= cap && N % bn == 0) return bn;
   return 0;
@@ -792,11 +788,11 @@ static int linear_kloop_bn(int N) {
 
 // Shared memory of the K-loop kernel: S stages of (x, W) chunks, YB output
 // staging buffers and the bias, the deepest pipeline first.  YB = 0 (rows
-// stored straight from registers, DCN_LINEAR_YB=0) frees the staging memory
+// stored straight from registers, the linear_yb switch at 0) frees the staging memory
 // for stages but measured slower (131072 x 512 -> 512: 96 us against 82 us).
 static size_t linear_kloop_smem(int BN, int N, int* S_out, int* YB_out) {
   const size_t sb = (size_t)(128 + BN) * 128, y = (size_t)128 * BN * 2;
-  const int ybmax = env_int_dev("DCN_LINEAR_YB", 2), smax = env_int_dev("DCN_LINEAR_S", 8);
+  const int ybmax = options().linear_yb, smax = options().linear_s;
   const int ybmin = ybmax == 0 ? 0 : 1;
   for (int S = smax; S >= 2; --S)
     for (int YB = ybmax; YB >= ybmin; --YB) {
@@ -870,13 +866,13 @@ static cudaError_t launch_linear_t(int dtype, long long M, int K, int N, const v
       int S = 0, YB = 0;
       // CTAs per SM: two when both fit (shared memory and 2 x 2 x tcols
       // tensor-memory columns), so that one CTA's epilogue overlaps the other's
-      int per_sm = env_int_dev("DCN_LINEAR_CTAS", 2) >= 2 && 4 * tcols <= 512 ? 2 : 1;
+      int per_sm = options().linear_ctas >= 2 && 4 * tcols <= 512 ? 2 : 1;
       size_t wsm = linear_ws_smem(K, N, &S, &YB, per_sm == 2 ? 113 * 1024 : 227 * 1024);
       if (!wsm && per_sm == 2) {
         per_sm = 1;
         wsm = linear_ws_smem(K, N, &S, &YB);
       }
-      if (wsm && 2 * tcols <= 512 && N % 64 == 0 && env_int_dev("DCN_LINEAR_PERSIST", 1)) {
+      if (wsm && 2 * tcols <= 512 && N % 64 == 0 && options().linear_persist) {
         cudaError_t e = cudaFuncSetAttribute(linear_ws_kernel<T>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)wsm);
         if (e != cudaSuccess) return e;

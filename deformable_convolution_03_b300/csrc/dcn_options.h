@@ -1,0 +1,44 @@
+// dcn_options.h -- the library's kernel-selection switches.
+//
+// Every field holds the production default.  The library never reads the
+// environment: the tests change a switch through dcn_internal_set_option (an
+// exported function that the public header does not declare) to run every
+// kernel instance and path against the oracle, and put it back afterwards.
+#pragma once
+
+namespace dcn {
+
+struct Options {
+  // forward
+  int fwd_wide = 1;       // 0: the general kernel instead of the wide one
+  int fwd_wide_cpt = 16;  // largest slice (channels) of the wide kernel
+  int fwd_cpt = 0;        // largest slice of the general kernel (0: one 16-byte vector)
+  int fwd_tile = 1;       // 2-D pixel tiles for the wide kernel
+  int fwd_tma = 1;        // the TMA-staged forward
+  int fwd_halo = 6;       // largest halo of the TMA forward's window
+  int fwd_any_tile = 1;   // tiles of any shape (else powers of two) for the TMA forward
+  int fwd_row64 = 1;      // 256-bit loads of merged 64-byte offset/mask rows
+  // backward
+  int bwd_split = 2;      // 2: split kernels for 16-bit storage, 1: for any dtype, 0: never
+  int bwd_fuse = 1;       // both split halves in one launch
+  int bwd_tma = 0;        // split sample blocks with TMA-staged windows
+  int bwd_tma_kb = 40;    // their window budget (KB)
+  int bwd_window = 2;     // 2: the window kernel for strides >= 2, 1: always, 0: never
+  int bwd_cpt = 4;        // largest slice of the single-pass kernel
+  int bwd_halo = 6;       // halo (pixels) of the split / window kernels' windows
+  int bwd_stage = 1;      // gradient rows staged in shared memory
+  // projections
+  int linear_tc = 1;       // tensor-core kernels where they apply
+  int linear_bn = 256;     // largest output tile width of the K-loop kernel
+  int linear_yb = 2;       // its output staging buffers
+  int linear_s = 8;        // its largest stage count
+  int linear_ctas = 2;     // persistent CTAs per SM when they fit
+  int linear_persist = 1;  // the persistent kernel where it applies
+  // a valid call reports DCN_ERR_CUDA before any CUDA call (error-path tests)
+  int fault_inject = 0;
+};
+
+// The switches in force (process-wide).
+const Options& options();
+
+}  // namespace dcn

@@ -1,3 +1,4 @@
+import ctypes
 import os
 import sys
 
@@ -25,3 +26,32 @@ def native():
     from deformable_convolution_03_b300 import build, binding
     build.build()
     return binding
+
+
+class Options:
+    """The library's kernel-selection switches (a test hook the library exports
+    without declaring it in its public header)."""
+
+    def __init__(self, lib):
+        self.lib = lib
+
+    def set(self, name: str, value: int) -> None:
+        rc = self.lib.dcn_internal_set_option(name.encode(), int(value))
+        assert rc == 0, f"unknown switch {name}"
+
+    def update(self, switches: dict) -> None:
+        for k, v in switches.items():
+            self.set(k, v)
+
+
+@pytest.fixture
+def opts(native):
+    """Switches set by a test, all put back to their defaults afterwards."""
+    L = native.lib()
+    L.dcn_internal_set_option.argtypes = [ctypes.c_char_p, ctypes.c_int]
+    L.dcn_internal_set_option.restype = ctypes.c_int
+    L.dcn_internal_reset_options.argtypes = []
+    L.dcn_internal_reset_options.restype = None
+    L.dcn_internal_reset_options()
+    yield Options(L)
+    L.dcn_internal_reset_options()

@@ -161,10 +161,10 @@ def test_empty_batch_is_a_no_op(native):
 
 
 @host_only
-def test_fault_hook_reports_cuda_error(native, monkeypatch):
+def test_fault_hook_reports_cuda_error(native, opts):
     lib = native.lib()
     p = native.Params(N=1, H=8, W=8, G=2, gc=4, dtype=native.DCN_F16)
-    monkeypatch.setenv("DCN_FAULT_INJECT", "launch")
+    opts.set("fault_inject", 1)
     assert lib.dcn_core_fwd(ctypes.byref(p.c()), A, A, A, A, None) == native.DCN_ERR_CUDA
     assert lib.dcn_core_bwd(ctypes.byref(p.c()), *([A] * 8), 1 << 30, None) == native.DCN_ERR_CUDA
     with pytest.raises(native.DCNError, match="DCN_ERR_CUDA"):

@@ -72,9 +72,9 @@ def test_tensor_core_k_loop_shapes(dt, M, K, N):
 
 
 @pytest.mark.parametrize("bn", ["64", "128"])
-def test_tensor_core_k_loop_narrow_tiles(bn, monkeypatch):
+def test_tensor_core_k_loop_narrow_tiles(bn, opts):
     # the same layer with its output split into 64- or 128-column tiles
-    monkeypatch.setenv("DCN_LINEAR_BN", bn)
+    opts.set("linear_bn", int(bn))
     _check(300, 512, 512, "bf16")
 
 
@@ -92,10 +92,10 @@ def test_full_size_projection_at_g_stage1():
 
 @pytest.mark.parametrize("dt", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("K,N", [(37, 13), (64, 16), (8, 300), (512, 96)])
-def test_cuda_core_path(dt, K, N, monkeypatch):
+def test_cuda_core_path(dt, K, N, opts):
     # shapes outside the tensor-core path, float32, and the tensor-core shapes
     # forced onto the CUDA-core kernel
-    monkeypatch.setenv("DCN_LINEAR_TC", "0")
+    opts.set("linear_tc", 0)
     _check(77, K, N, dt)
 
 

@@ -30,18 +30,17 @@ CASES = [
 
 BWD = {
     "default": {},
-    "split": {"DCN_BWD_SPLIT": "1"},
-    "split_tma": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1"},
-    "single_pass": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "0"},
+    "split": {"bwd_split": 1},
+    "split_tma": {"bwd_split": 1, "bwd_tma": 1},
+    "single_pass": {"bwd_split": 0, "bwd_window": 0},
 }
 
 
 @pytest.mark.parametrize("bwd", list(BWD))
 @pytest.mark.parametrize("name,over,stride", CASES, ids=[c[0] for c in CASES])
-def test_merged_layout_forward_and_backward(name, over, stride, bwd, monkeypatch):
+def test_merged_layout_forward_and_backward(name, over, stride, bwd, opts):
     # every backward path reads the merged rows and writes their padding
-    for k, v in BWD[bwd].items():
-        monkeypatch.setenv(k, v)
+    opts.update(BWD[bwd])
     w = WORKLOADS[name].with_(backward=True, **over)
     t = make_inputs(w, grad=True)
     p = lib_params(w)

@@ -105,13 +105,10 @@ def test_small_forward_and_backward(w):
 
 @pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("cap", [1, 2, 4, 8, 16, 32])
-def test_every_general_kernel_instance(dt, cap, monkeypatch):
+def test_every_general_kernel_instance(dt, cap, opts):
     # force each channels-per-thread instance of the general kernels
-    monkeypatch.setenv("DCN_FWD_WIDE", "0")
-    monkeypatch.setenv("DCN_BWD_SPLIT", "0")
-    monkeypatch.setenv("DCN_BWD_WINDOW", "0")
-    monkeypatch.setenv("DCN_FWD_CPT", str(cap))
-    monkeypatch.setenv("DCN_BWD_CPT", str(cap))
+    opts.update({"fwd_wide": 0, "bwd_split": 0, "bwd_window": 0,
+                 "fwd_cpt": cap, "bwd_cpt": cap})
     w = small(f"inst_{dt}_{cap}", dt, gc=32, G=2, softmax=1, N=3, H=10, W=9)
     t = make_inputs(w)
     check_fwd(w, t)
@@ -122,11 +119,10 @@ def test_every_general_kernel_instance(dt, cap, monkeypatch):
 @pytest.mark.parametrize("gc", [4, 8, 16, 24, 48])
 @pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
 @pytest.mark.parametrize("tile", ["1", "0"])
-def test_wide_forward_instances(dt, gc, sm, rc, tile, monkeypatch):
+def test_wide_forward_instances(dt, gc, sm, rc, tile, opts):
     # slices of 4, 8 and 16 channels, 9 points and the runtime point count,
     # blocks over 2-D pixel tiles and over consecutive items
-    monkeypatch.setenv("DCN_FWD_TMA", "0")
-    monkeypatch.setenv("DCN_FWD_TILE", tile)
+    opts.update({"fwd_tma": 0, "fwd_tile": int(tile)})
     w = small(f"wide_{dt}_{gc}", dt, gc=gc, G=3, softmax=sm, remove_center=rc, N=2, H=11, W=13)
     check_fwd(w, make_inputs(w))
 
@@ -135,12 +131,12 @@ def test_wide_forward_instances(dt, gc, sm, rc, tile, monkeypatch):
 @pytest.mark.parametrize("gc,G", [(8, 4), (16, 4), (16, 8), (32, 4), (48, 2)])
 @pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
 @pytest.mark.parametrize("halo", ["6", "2", "0"])
-def test_tma_forward_instances(dt, gc, G, sm, rc, halo, monkeypatch):
+def test_tma_forward_instances(dt, gc, G, sm, rc, halo, opts):
     # the forward with its input window staged by a tensor copy: every slice
     # width, one or several blocks per tile's groups (a pixel's channels over
     # 128 bytes), the 9-point, 8-point and runtime instances; halos of 6, 2
     # and 0 pixels send more and more samples through the far path
-    monkeypatch.setenv("DCN_FWD_HALO", halo)
+    opts.set("fwd_halo", int(halo))
     w = small(f"tma_{dt}_{gc}_{G}", dt, gc=gc, G=G, softmax=sm, remove_center=rc, N=2, H=19,
               W=21, offset_std=3.0)
     check_fwd(w, make_inputs(w))
@@ -186,43 +182,43 @@ SPLIT = [
 
 
 BWD_MODES = {
+    # the default path
+    "default": {},
     # the split kernels (sample kernel + windowed input kernel), every dtype
-    "split": {"DCN_BWD_SPLIT": "1"},
+    "split": {"bwd_split": 1},
     # the same with a one-pixel halo: most samples leave the window and take
     # the far path
-    "split_halo1": {"DCN_BWD_SPLIT": "1", "DCN_BWD_HALO": "1"},
+    "split_halo1": {"bwd_split": 1, "bwd_halo": 1},
     # the split kernels with gradient rows written straight to memory and the
     # sample kernel over consecutive items instead of tiles
-    "split_direct": {"DCN_BWD_SPLIT": "1", "DCN_BWD_STAGE": "0", "DCN_FWD_TILE": "0"},
+    "split_direct": {"bwd_split": 1, "bwd_stage": 0, "fwd_tile": 0},
     # the two split kernels as separate launches instead of one
-    "split_unfused": {"DCN_BWD_SPLIT": "1", "DCN_BWD_FUSE": "0"},
+    "split_unfused": {"bwd_split": 1, "bwd_fuse": 0},
     # the fused launch with the sample blocks' input windows staged by a
     # tensor copy, with a small window (many far samples)
-    "split_tma": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1"},
-    "split_tma_small": {"DCN_BWD_SPLIT": "1", "DCN_BWD_TMA": "1", "DCN_BWD_TMA_KB": "8"},
+    "split_tma": {"bwd_split": 1, "bwd_tma": 1},
+    "split_tma_small": {"bwd_split": 1, "bwd_tma": 1, "bwd_tma_kb": 8},
     # the fused windowed kernel, with its default halo and with one pixel
-    "window": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1"},
-    "window_halo1": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "1", "DCN_BWD_HALO": "1"},
+    "window": {"bwd_split": 0, "bwd_window": 1},
+    "window_halo1": {"bwd_split": 0, "bwd_window": 1, "bwd_halo": 1},
     # the single-pass atomic kernels
-    "single_pass": {"DCN_BWD_SPLIT": "0", "DCN_BWD_WINDOW": "0"},
+    "single_pass": {"bwd_split": 0, "bwd_window": 0},
 }
 
 
 @pytest.mark.parametrize("w", SPLIT, ids=lambda w: w.name)
 @pytest.mark.parametrize("mode", list(BWD_MODES))
-def test_backward_paths(w, mode, monkeypatch):
-    for k, v in BWD_MODES[mode].items():
-        monkeypatch.setenv(k, v)
+def test_backward_paths(w, mode, opts):
+    opts.update(BWD_MODES[mode])
     check_bwd(w, make_inputs(w))
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 @pytest.mark.parametrize("mode", ["split", "window", "single_pass"])
-def test_backward_crowded_samples(dt, mode, monkeypatch):
+def test_backward_crowded_samples(dt, mode, opts):
     # every sample of a 32x32 image aimed at one cell: the cells inside each
     # tile's window collect hundreds of samples, the rest leave the window
-    for k, v in BWD_MODES[mode].items():
-        monkeypatch.setenv(k, v)
+    opts.update(BWD_MODES[mode])
     w = small(f"crowd_{dt}", dt, gc=16, G=1, N=1, H=32, W=32, softmax=1)
     t = make_inputs(w)
     ho = torch.arange(w.H_out).view(-1, 1, 1)
