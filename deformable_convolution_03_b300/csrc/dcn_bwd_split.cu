@@ -112,6 +112,8 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
 #pragma unroll
     for (int i = 0; i < NW; ++i) gw[i] = 0u;
   }
+  Halves<NW> gh;
+  if constexpr (sizeof(T) == 2) gh.split(gw);
 
   // separate offset / mask tensors and a compile-time point count: the rows
   // with a few aligned vector loads
@@ -191,7 +193,7 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
       float s[2] = {0.f, 0.f};
       if constexpr (sizeof(T) == 2) {
 #pragma unroll
-        for (int i = 0; i < NW; ++i) dot_word<T>(s[0], s[1], v[k][i], gw[i]);
+        for (int i = 0; i < NW; ++i) dot_split<T>(s[0], s[1], v[k][i], gh.lo[i], gh.hi[i]);
       } else {
 #pragma unroll
         for (int i = 0; i < NW; ++i)
@@ -341,6 +343,8 @@ __device__ __forceinline__ void sample_block_tma(const CUtensorMap* tmap, const 
     for (int i = 0; i < NW; ++i) gw[i] = 0u;
   }
   rotate_chunks<NW>(gw, rot);
+  Halves<NW> gh;
+  if constexpr (sizeof(T) == 2) gh.split(gw);
 
   UnitRows<T, KP> rows;
   bool vec = false;
@@ -426,7 +430,7 @@ __device__ __forceinline__ void sample_block_tma(const CUtensorMap* tmap, const 
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if constexpr (sizeof(T) == 2) {
-              dot_word<T>(s2[0], s2[1], cw4[e], gw[4 * j + e]);
+              dot_split<T>(s2[0], s2[1], cw4[e], gh.lo[4 * j + e], gh.hi[4 * j + e]);
             } else {
               s2[e & 1] = fmaf(__uint_as_float(gw[4 * j + e]), __uint_as_float(cw4[e]), s2[e & 1]);
             }
@@ -451,7 +455,7 @@ __device__ __forceinline__ void sample_block_tma(const CUtensorMap* tmap, const 
         float s2[2] = {0.f, 0.f};
         if constexpr (sizeof(T) == 2) {
 #pragma unroll
-          for (int i = 0; i < NW; ++i) dot_word<T>(s2[0], s2[1], v[i], gw[i]);
+          for (int i = 0; i < NW; ++i) dot_split<T>(s2[0], s2[1], v[i], gh.lo[i], gh.hi[i]);
         } else {
 #pragma unroll
           for (int i = 0; i < NW; ++i)
@@ -677,40 +681,6 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
       far |= 1u << p;
     }
   }
-  // far samples (rare): the point again, its four corners straight to memory
-  while (far) {
-    const int p = __ffs(far) - 1;
-    far &= far - 1;
-    float m = Dt<T>::one(mrow + p);
-    if (kp.softmax) m = expf(m - mx) * inv;
-    const float2 d = Dt<T>::two(orow + 2 * p);
-    const float x = location(d.x, kp.tap_x[p], scale, ref_x);
-    const float y = location(d.y, kp.tap_y[p], scale, ref_y);
-    const float xf = floorf(x), yf = floorf(y);
-    const int x0 = (int)xf, y0 = (int)yf;
-    const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
-    const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
-    const uint4* src = reinterpret_cast<const uint4*>(gos + local * NW);
-    float gof[CPT];
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const uint4 u = src[c ^ swz(local)];
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) Dt<T>::unpack(wd[i], gof + (4 * c + i) * Dt<T>::kPerWord);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
-      if ((unsigned)yy >= (unsigned)H || (unsigned)xx >= (unsigned)W) continue;
-      float* dst = gin + img_off + ((size_t)yy * W + xx) * kp.C;
-#pragma unroll
-      for (int i = 0; i < CPT; i += 4)
-        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i),
-                     "f"(w[c] * gof[i]), "f"(w[c] * gof[i + 1]), "f"(w[c] * gof[i + 2]),
-                     "f"(w[c] * gof[i + 3]));
-    }
-  }
   __syncthreads();
 
   // ---- pass 2: list heads (block-wide exclusive scan), then each sample to
@@ -868,6 +838,51 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
       float* dst = gin + img_off + (size_t)off * kp.C + 4 * j;
       asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[4 * r]),
                    "f"(acc[4 * r + 1]), "f"(acc[4 * r + 2]), "f"(acc[4 * r + 3]));
+    }
+  }
+  // far samples (rare): the point again, its four corners straight to memory.
+  // Done last, so that no barrier of the passes above waits for these
+  // reductions.
+  if (far) {
+    if (kp.softmax) {
+      mx = -INFINITY;
+      for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
+      float s = 0.f;
+      for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
+      inv = 1.f / s;
+    }
+    while (far) {
+      const int p = __ffs(far) - 1;
+      far &= far - 1;
+      float m = Dt<T>::one(mrow + p);
+      if (kp.softmax) m = expf(m - mx) * inv;
+      const float2 d = Dt<T>::two(orow + 2 * p);
+      const float x = location(d.x, kp.tap_x[p], scale, ref_x);
+      const float y = location(d.y, kp.tap_y[p], scale, ref_y);
+      const float xf = floorf(x), yf = floorf(y);
+      const int x0 = (int)xf, y0 = (int)yf;
+      const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
+      const float w[4] = {gy * gx * m, gy * fx * m, fy * gx * m, fy * fx * m};
+      const uint4* src = reinterpret_cast<const uint4*>(gos + local * NW);
+      float gof[CPT];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const uint4 u = src[c ^ swz(local)];
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) Dt<T>::unpack(wd[i], gof + (4 * c + i) * Dt<T>::kPerWord);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
+        if ((unsigned)yy >= (unsigned)H || (unsigned)xx >= (unsigned)W) continue;
+        float* dst = gin + img_off + ((size_t)yy * W + xx) * kp.C;
+#pragma unroll
+        for (int i = 0; i < CPT; i += 4)
+          asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i),
+                       "f"(w[c] * gof[i]), "f"(w[c] * gof[i + 1]), "f"(w[c] * gof[i + 2]),
+                       "f"(w[c] * gof[i + 3]));
+      }
     }
   }
 }

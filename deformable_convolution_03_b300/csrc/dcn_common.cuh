@@ -487,6 +487,39 @@ __device__ __forceinline__ void dot_word<__nv_bfloat16>(float& s0, float& s1, ui
       : "+f"(s0), "+f"(s1) : "r"(v), "r"(g));
 }
 
+// The 16-bit halves of the words of a grad_out slice, split once so that the
+// dot products below split only the sampled words.
+template <int NW>
+struct Halves {
+  unsigned short lo[NW], hi[NW];
+  __device__ __forceinline__ void split(const uint32_t (&w)[NW]) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) asm("mov.b32 {%0, %1}, %2;" : "=h"(lo[i]), "=h"(hi[i]) : "r"(w[i]));
+  }
+};
+
+// s0 += lo(v) * g0, s1 += hi(v) * g1: the dot product of a packed 16-bit pair
+// with two grad_out halves already split, each product exact in float32.
+template <typename T>
+__device__ __forceinline__ void dot_split(float& s0, float& s1, uint32_t v, unsigned short g0,
+                                          unsigned short g1);
+
+template <>
+__device__ __forceinline__ void dot_split<__half>(float& s0, float& s1, uint32_t v,
+                                                  unsigned short g0, unsigned short g1) {
+  asm("{\n\t.reg .b16 vl, vh;\n\tmov.b32 {vl, vh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, vl, %3, %0;\n\tfma.rn.f32.f16 %1, vh, %4, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(v), "h"(g0), "h"(g1));
+}
+
+template <>
+__device__ __forceinline__ void dot_split<__nv_bfloat16>(float& s0, float& s1, uint32_t v,
+                                                         unsigned short g0, unsigned short g1) {
+  asm("{\n\t.reg .b16 vl, vh;\n\tmov.b32 {vl, vh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, vl, %3, %0;\n\tfma.rn.f32.bf16 %1, vh, %4, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(v), "h"(g0), "h"(g1));
+}
+
 template <typename T, int NW>
 __device__ __forceinline__ void fma_words(float* acc, const uint32_t (&v)[NW], typename Fma<T>::W w) {
   if constexpr (sizeof(T) == 2) {
