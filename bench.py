@@ -53,14 +53,15 @@ METRIC = "DCN core fwd/bwd GB/s and % of HBM roofline; images/s at FlashInternIm
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6400.0
 
-# DRAM traffic per launch from an ncu capture (profiles/), keyed by kernel and
-# workload, with the sha1 of the kernel source it was taken on: a changed
-# source voids the figure.
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from
+# an ncu capture of the same workload), keyed by kernel and workload, with the
+# sha1 of the kernel sources it was taken on: a changed source voids the
+# figure.
 TRAFFIC = {
-    # profiles/launches_t_stage1_f16.md: fwd_tile_kernel, per launch
+    # fwd_tile_kernel, per launch
     "fwd@t_stage1_f16": {"bytes": 69_082_390 + 851_812, "sha": "47abd65c757c"},
-    # profiles/launches_t_stage1_f16.md: bwd_both_kernel + round_kernel, per
-    # call (the accumulator's memset is not a kernel and is not counted)
+    # bwd_both_kernel + round_kernel, per call (the accumulator's memset is not
+    # a kernel and is not counted)
     "bwd@t_stage1_f16": {"bytes": 169_791_521 + 44_494_893 + 51_389_229 + 112_952,
                          "sha": "932930369705"},
 }
@@ -444,7 +445,11 @@ class OracleTimer:
         self.perm = np.random.default_rng(1234).permutation(self.total)
         ib = ideal_bytes(w)
         self.step_bytes = ib["fwd"] + ib["bwd"]
-        self.cores = oracle.max_threads()
+        self.cores = self.all_cores = oracle.max_threads()
+
+    def set_cores(self, n: int) -> None:
+        self.o.set_threads(n)
+        self.cores = n
 
     def run(self, npix: int) -> float:
         pix = self.perm[:npix]
@@ -492,7 +497,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ot.step_bytes / (value * 1e9) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_of(w, args.gpus),
+        "data": "synthetic", "config": {**config_of(w, args.gpus), "layout": args.layout},
         "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": ot.cores,
                          "kind": "oracle",
                          "sample": "each step: " + ot.describe(npix, total_t / len(times))},
@@ -641,7 +646,15 @@ def main():
         dt = ot.run(npix)
         line["cpu_baseline"] = {"value": round(ot.gbs(npix, dt), 5), "unit": UNIT,
                                 "cores": ot.cores, "kind": "oracle",
-                                "sample": ot.describe(npix, dt)}
+                                "sample": ot.describe(npix, dt),
+                                "nproc": os.cpu_count()}
+        # the same oracle on one core, on a sample sized for the same budget
+        ot.set_cores(1)
+        n1 = ot.size_for(args.cpu_budget / 2)
+        dt1 = ot.run(n1)
+        line["cpu_baseline"]["one_core"] = {"value": round(ot.gbs(n1, dt1), 5), "unit": UNIT,
+                                            "cores": 1, "sample": ot.describe(n1, dt1)}
+        ot.set_cores(ot.all_cores)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

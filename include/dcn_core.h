@@ -107,7 +107,11 @@ int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset,
  * Returns 0 as well when the parameters are invalid. */
 size_t dcn_core_bwd_workspace(const dcn_params_t* p);
 
-/* Backward of L = <grad_out, output>: the analytic derivative of the forward.
+/* Backward of L = <grad_out, output>: the analytic derivative of the forward
+ * (the walkthrough's steps 2-5 differentiated; the fused kernel's backward and
+ * the memory of its sampling intermediates are discussed on the page
+ * "简介这是一份面向图像分类任务实战的FlashInternImage模型资源包", sections 2.2
+ * and 5.2, whose kernels recompute the locations instead of storing them).
  *   grad_input  (N, H, W, G*gc)          dL/d input, fully overwritten
  *   grad_offset (N, H_out, W_out, G, P, 2)  dL/d offset, fully overwritten
  *   grad_mask   (N, H_out, W_out, G, P)  dL/d mask; with softmax this is the
