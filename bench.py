@@ -53,17 +53,35 @@ METRIC = "DCN core fwd/bwd GB/s and % of HBM roofline; images/s at FlashInternIm
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6400.0
 
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum from
-# an ncu capture of the same workload), keyed by kernel and workload, with the
-# sha1 of the kernel sources it was taken on: a changed source voids the
-# figure.
+# DRAM traffic per call (dram__bytes_read.sum + dram__bytes_write.sum of the
+# call's kernels in an ncu capture of `bench.py --profile-step --workload W`),
+# keyed by phase and workload, with the sha1 of the kernel sources it was
+# taken on: a changed source voids the figure.  The backward's memset of its
+# float32 accumulator is not a kernel and is not counted.
+FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
+BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
+_F, _B = "49f576c5c777", "c048ad1b714f"
 TRAFFIC = {
-    # fwd_tile_kernel, per launch
-    "fwd@t_stage1_f16": {"bytes": 69_082_390 + 851_812, "sha": "47abd65c757c"},
-    # bwd_both_kernel + round_kernel, per call (the accumulator's memset is not
-    # a kernel and is not counted)
-    "bwd@t_stage1_f16": {"bytes": 169_791_521 + 44_494_893 + 51_389_229 + 112_952,
-                         "sha": "932930369705"},
+    "fwd@v3_tiny_f32": {"bytes": 47_616, "sha": _F},
+    "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_131_328, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_478_912, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_020_736, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 269_369_344, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_676_480, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_266_432, "sha": _B},
+    "fwd@t_stage3_bf16": {"bytes": 17_298_432, "sha": _F},
+    "bwd@t_stage3_bf16": {"bytes": 49_478_912, "sha": _B},
+    "fwd@t_stage4_bf16": {"bytes": 8_668_416, "sha": _F},
+    "bwd@t_stage4_bf16": {"bytes": 24_794_624, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_417_664, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 311_189_760, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_055_360, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_576_704, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 73_142_016, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_217_536, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_058_432, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_575_296, "sha": _B},
 }
 
 
@@ -508,6 +526,53 @@ def run_reference(args, rank, world):
     return 0
 
 
+def profile_step(w: Workload, dev, layout: str) -> int:
+    """One step of the workload bracketed for a profiler started with
+    --profile-from-start off (after two warm-up steps)."""
+    case = Case(w, dev, 0, layout)
+    for _ in range(2):
+        case.fwd()
+        case.bwd()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    case.fwd()
+    case.bwd()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    return 0
+
+
+def profile_proj(dev) -> int:
+    """The layers around the core, one call each bracketed for a profiler:
+    FlashInternImage-T stage 1's merged offset/mask projection (200704 x 64 ->
+    128) and output projection (-> 64) in float16, InternImage-G stage 1's
+    512 -> 512 projection (32768 rows) in bfloat16, and the centre feature
+    scale forward and backward at stage 1 (200704 x 64, 4 gates, float16)."""
+    g = torch.Generator().manual_seed(1)
+    calls = []
+    for M, K, N, dt in ((200704, 64, 128, torch.float16), (200704, 64, 64, torch.float16),
+                        (32768, 512, 512, torch.bfloat16)):
+        x = (torch.rand(M, K, generator=g) * 2 - 1).to(dt).to(dev)
+        wt = (torch.randn(N, K, generator=g) / K ** 0.5).to(dt).to(dev)
+        b = torch.randn(N, generator=g).to(dt).to(dev)
+        calls.append(lambda x=x, wt=wt, b=b: B.linear(x, wt, b))
+    M, C, G = 200704, 64, 4
+    core, xp, go = ((torch.rand(M, C, generator=g) * 2 - 1).half().to(dev) for _ in range(3))
+    lg = torch.randn(M, G, generator=g).half().to(dev)
+    calls.append(lambda: B.center_feature_scale(core, xp, lg))
+    calls.append(lambda: B.center_feature_scale_backward(go, core, xp, lg))
+    for f in calls:
+        f()
+        f()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    for f in calls:
+        f()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    return 0
+
+
 def config_of(w: Workload, n: int) -> dict:
     return {"workload": w.name,
             "shape": f"N={w.N} H=W={w.H} C={w.C} G={w.G} gc={w.gc} k{w.kernel_h}x{w.kernel_w} "
@@ -534,6 +599,13 @@ def main():
     ap.add_argument("--no-stages", action="store_true", help="skip the T-stage images/s sweep")
     ap.add_argument("--no-proj", action="store_true",
                     help="skip the projections around the core (dcn_linear)")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="for a profiler: two warm-up steps, then one step (forward + backward) "
+                         "between cudaProfilerStart and cudaProfilerStop; no timing")
+    ap.add_argument("--profile-proj", action="store_true",
+                    help="for a profiler: the projections and the centre feature scale around the "
+                         "core, two warm-up calls each, then one call each between "
+                         "cudaProfilerStart and cudaProfilerStop")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=8.0)
     args = ap.parse_args()
@@ -555,6 +627,10 @@ def main():
     torch.cuda.set_device(dev)
 
     w = WORKLOADS[args.workload]
+    if args.profile_step:
+        return profile_step(w.with_(backward=True), dev, args.layout)
+    if args.profile_proj:
+        return profile_proj(dev)
     case = Case(w, dev, rank, args.layout)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -610,12 +686,12 @@ def main():
     roof = {
         "bwd": {"bound": "hbm", "achieved": round(bwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(bwd_gbs / peak, 4),
-                "traffic": traffic_for(f"bwd@{w.name}", ("dcn_bwd_split.cu", "dcn_bwd.cu")) if args.layout == "separate" else None,
+                "traffic": traffic_for(f"bwd@{w.name}", BWD_SRCS) if args.layout == "separate" else None,
                 "phase": "dcn_core_bwd: workspace memset + bwd_both_kernel + round_kernel",
                 "ms": round(bwd_ms, 5), "peak_source": f"{peak_kind} HBM copy bandwidth"},
         "fwd": {"bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(fwd_gbs / peak, 4),
-                "traffic": traffic_for(f"fwd@{w.name}", ("dcn_fwd_tma.cu",)) if args.layout == "separate" else None,
+                "traffic": traffic_for(f"fwd@{w.name}", FWD_SRCS) if args.layout == "separate" else None,
                 "phase": "dcn_core_fwd: fwd_tile_kernel (TMA-staged)", "ms": round(fwd_ms, 5),
                 "peak_source": f"{peak_kind} HBM copy bandwidth"},
     }

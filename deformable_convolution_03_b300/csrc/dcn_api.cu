@@ -301,67 +301,6 @@ int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const 
   return 0;
 }
 
-// The windowed backward: channels per lane 16, 8 or 4 (slices of 16 to 64
-// bytes, gc/c a power of two no larger than 32), at most 16 points, 256
-// threads per CTA; the tile is 16 output pixels wide where the output allows;
-// the window covers the tile's footprint plus a halo of R pixels for the
-// offsets, R from 6 down to 1 so that the shared memory stays within 64 KB
-// (three CTAs per SM).  Returns c with *wg filled, or 0 to use the single-pass
-// kernels.
-//
-// Used by default for strided convolutions only.  Measured on B300: at stride
-// 2 / dilation 2 (64 x 28^2 x 128, fp32) it takes 68 us against 170 us for the
-// single-pass kernel; at stride 1 the window's shared memory takes L1
-// capacity away from the corner gathers and it is slower (FlashInternImage-T
-// stage 1: 588 us against 430 us).  The bwd_window switch at 1 uses it for every
-// geometry it can take, 0 never.
-constexpr size_t kWindowSmem = 64 * 1024;
-
-int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const void* gout,
-                const void* acc, dcn::WinGeom* wg) {
-  const int mode = dcn::options().bwd_window;
-  if (mode == 0) return 0;
-  if (mode != 1 && p->stride_h < 2 && p->stride_w < 2) return 0;
-  const int es = elem_size(p->dtype);
-  if (g.P > 16 || (long long)p->H * p->W * p->G * p->gc >= (1LL << 31) || !aligned(acc, 16))
-    return 0;
-  int cpt = 0;
-  for (int c = 16; c >= 4; c >>= 1) {
-    const int bytes = c * es, chunks = p->gc / c;
-    if (p->gc % c || bytes < 16 || bytes > 64) continue;
-    if (chunks > 32 || (chunks & (chunks - 1))) continue;
-    const size_t a = bytes >= 32 ? 32 : 16;
-    if (aligned(in, a) && aligned(gout, a)) { cpt = c; break; }
-  }
-  if (!cpt) return 0;
-  auto pow2_at_least = [](int v) { int r = 1; while (r < v) r <<= 1; return r; };
-  const int nunit = 256 / (p->gc / cpt);
-  int TW = pow2_at_least(g.Wo) < 16 ? pow2_at_least(g.Wo) : 16;
-  if (TW > nunit) TW = nunit;
-  const int TH = nunit / TW;
-  const double os = p->offset_scale;
-  const int cw = p->dilation_w * (p->kernel_w - 1) / 2, ch = p->dilation_h * (p->kernel_h - 1) / 2;
-  const double x0 = -cw * os, x1 = ((p->kernel_w - 1) * p->dilation_w - cw) * os;
-  const double y0 = -ch * os, y1 = ((p->kernel_h - 1) * p->dilation_h - ch) * os;
-  const int tmin_x = (int)std::floor(x0 < x1 ? x0 : x1), tmax_x = (int)std::ceil(x0 < x1 ? x1 : x0);
-  const int tmin_y = (int)std::floor(y0 < y1 ? y0 : y1), tmax_y = (int)std::ceil(y0 < y1 ? y1 : y0);
-  for (int R = dcn::options().bwd_halo; R >= 1; --R) {
-    wg->TH = TH;
-    wg->TW = TW;
-    wg->WH = (TH - 1) * p->stride_h + (tmax_y - tmin_y) + 2 * R + 2;
-    wg->WW = (TW - 1) * p->stride_w + (tmax_x - tmin_x) + 2 * R + 2;
-    wg->org_y = -p->pad_h + ch + tmin_y - R;
-    wg->org_x = -p->pad_w + cw + tmin_x - R;
-    wg->tiles_h = (g.Ho + TH - 1) / TH;
-    wg->tiles_w = (g.Wo + TW - 1) / TW;
-    if (dcn::window_smem_bytes(*wg, g.P, p->gc, es) <= kWindowSmem) {
-      if ((long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
-      return cpt;
-    }
-  }
-  return 0;
-}
-
 // The split backward: a sample kernel shaped like the wide forward (same
 // channels per thread and tiles, chosen here into *kp) and an input kernel
 // over windows, one thread per output pixel of a TH x TW <= 256 tile of one
@@ -376,17 +315,15 @@ int plan_window(const dcn_params_t* p, const Geometry& g, const void* in, const 
 // Used by default for 16-bit storage, where it measured fastest on B300
 // (FlashInternImage-T stage 1, fp16: 308 us against 436 us for the
 // single-pass kernel; InternImage-G stage 1, bf16: 391 us against 539 us for
-// the fused window kernel).  For float32 the corner gathers of the sample
-// kernel cost twice as much and the single-pass or window kernels win
-// (64 x 28^2 x 128: 348 us against 227 us).  The bwd_split switch at 1 uses it for every
-// dtype it can take, 0 never.
+// a fused window kernel since removed).  For float32 the corner gathers of
+// the sample kernel cost twice as much and the single-pass kernel wins
+// (64 x 28^2 x 128: 348 us against 227 us).  The bwd_split switch at 1 uses it
+// for every dtype it can take, 0 never.
 constexpr size_t kSplitSmem = 56 * 1024;
 constexpr size_t kStageSmem = 32 * 1024;
 
 int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const void* gout,
-               const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb,
-               dcn::TileGeom* tg, void* map, bool* tma) {
-  *tma = false;
+               const void* acc, dcn::KParams* kp, dcn::WinGeom* wg, int* la, int* lb) {
   const int mode = dcn::options().bwd_split;
   if (mode == 0 || (mode != 1 && p->dtype == DCN_F32)) return 0;
   const int es = elem_size(p->dtype);
@@ -431,16 +368,10 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
   }
   if (best < 0 || (long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
   // the sample blocks read their corners through L1 over the wide forward's
-  // tiles.  The bwd_tma switch stages their input windows by a tensor copy
-  // instead (the forward's TMA plan, windows within bwd_tma_kb KB): measured
-  // slower inside the fused launch (FlashInternImage-T stage 1: 315-326 us
-  // against 272 us), whose input blocks then get less L1.
-  const bool fused = dcn::options().bwd_fuse != 0;
-  const size_t tma_budget = (size_t)dcn::options().bwd_tma_kb * 1024;
-  if (fused && dcn::options().bwd_tma && plan_fwd_tile(p, g, cpt, in, kp, tg, map, tma_budget))
-    *tma = true;
-  else
-    plan_fwd_tiles(p, g, cpt, kp);
+  // tiles (staging their windows by a tensor copy measured slower inside the
+  // fused launch: FlashInternImage-T stage 1 315-326 us against 272 us, the
+  // input blocks then getting less L1)
+  plan_fwd_tiles(p, g, cpt, kp);
   // grad_offset / grad_mask rows staged in shared memory
   const int ub = 256 / chunks;
   if (kp->merged) {
@@ -451,9 +382,6 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     *lb = g.P;
   }
   if (!dcn::options().bwd_stage || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
-  // staged rows are copied out per tile row, which needs every group of a
-  // pixel in the block
-  if (*tma && tg->GB != p->G) *la = *lb = 0;
   return cpt;
 }
 
@@ -581,12 +509,8 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
   }
   dcn::WinGeom wg;
   int la = 0, lb = 0;
-  dcn::TileGeom tg;
-  alignas(64) unsigned char map[128];
-  bool tma = false;
-  const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb, &tg, map, &tma);
-  const int wcpt = scpt ? 0 : plan_window(p, g, input, grad_out, acc, &wg);
-  const int cpt = scpt || wcpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
+  const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb);
+  const int cpt = scpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
   if (fault_injected()) return DCN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (g.n_in > 0) {
@@ -596,10 +520,7 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
   if (scpt)
     return cuda_status(dcn::launch_bwd_split(kp, wg, p->dtype, scpt, la, lb, grad_out, input,
                                              offset, mask, acc, grad_input, grad_offset,
-                                             grad_mask, tma ? map : nullptr, &tg, s));
-  if (wcpt)
-    return cuda_status(dcn::launch_bwd_window(kp, wg, p->dtype, wcpt, grad_out, input, offset,
-                                              mask, acc, grad_input, grad_offset, grad_mask, s));
+                                             grad_mask, s));
   return cuda_status(dcn::launch_bwd(kp, p->dtype, cpt, grad_out, input, offset, mask, acc,
                                      grad_input, grad_offset, grad_mask, s));
 }
@@ -678,12 +599,11 @@ int dcn_version(void) { return 100; }
 
 int dcn_wait_timeouts(unsigned long long* count) {
   if (!count) return DCN_ERR_NULL;
-  unsigned long long a = 0, b = 0, c = 0;
+  unsigned long long a = 0, c = 0;
   if (dcn::read_wait_timeouts(&a) != cudaSuccess ||
-      dcn::read_split_wait_timeouts(&b) != cudaSuccess ||
       dcn::read_linear_wait_timeouts(&c) != cudaSuccess)
     return DCN_ERR_CUDA;
-  *count = a + b + c;
+  *count = a + c;
   return DCN_OK;
 }
 
@@ -767,9 +687,6 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_row64", &dcn::Options::fwd_row64},
     {"bwd_split", &dcn::Options::bwd_split},
     {"bwd_fuse", &dcn::Options::bwd_fuse},
-    {"bwd_tma", &dcn::Options::bwd_tma},
-    {"bwd_tma_kb", &dcn::Options::bwd_tma_kb},
-    {"bwd_window", &dcn::Options::bwd_window},
     {"bwd_cpt", &dcn::Options::bwd_cpt},
     {"bwd_halo", &dcn::Options::bwd_halo},
     {"bwd_stage", &dcn::Options::bwd_stage},

@@ -271,250 +271,6 @@ bwd_sample_kernel(const KParams kp, const T* __restrict__ gout, const T* __restr
 }
 
 
-// The sample half with the input window staged by a tensor copy, as the
-// TMA-staged forward (dcn_fwd_tma.cu) does: a block covers the tile of kp for
-// GB groups (tg), one copy brings the window of input pixels its samples can
-// reach, zero-filled outside the image, and corners of in-window cells are
-// read from shared memory; far samples read clamped corners from global
-// memory.  grad_out's chunks are rotated once per thread like the corners
-// (d_k is a sum over all channels, so the order does not matter).  Gradient
-// rows are staged in shared memory after the window when the block covers
-// all groups of its pixels (la > 0; whole tile rows are then contiguous in
-// memory), else written directly.  The wait is bounded as in the forward.
-__device__ unsigned long long g_split_wait_timeouts = 0;
-constexpr int kSplitWaitPolls = 1 << 22;
-
-template <typename T, int CPT, int KP>
-__device__ __forceinline__ void sample_block_tma(const CUtensorMap* tmap, const KParams& kp,
-                                                 const TileGeom& tg,
-                                                 const T* __restrict__ gout,
-                                                 const T* __restrict__ input,
-                                                 const T* __restrict__ offset,
-                                                 const T* __restrict__ mask,
-                                                 T* __restrict__ goff, T* __restrict__ gmask,
-                                                 int la, int lb, const unsigned bid) {
-  constexpr int NW = CPT * (int)sizeof(T) / 4;
-  constexpr int NC = NW / 4;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + tg.win_bytes);
-  T* s_rows = reinterpret_cast<T*>(smem + tg.win_bytes + 16);
-  const int chunks = kp.gc / CPT;
-  const int P = KP > 0 ? KP : kp.P;
-
-  const int gb = bid % tg.ngb;
-  const int rest = bid / tg.ngb;
-  const int tiles = kp.tiles_w * kp.tiles_h;
-  const int t = rest % tiles;
-  const uint32_t n = rest / tiles;
-  const int ty = t / kp.tiles_w;
-  const int ho0 = ty * kp.tile_h, wo0 = (t - ty * kp.tiles_w) * kp.tile_w;
-  const int wy0 = ho0 * kp.stride_h + tg.org_y, wx0 = wo0 * kp.stride_w + tg.org_x;
-
-  if (threadIdx.x == 0) mbar_init(bar, 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mbar_expect_tx(bar, tg.win_bytes);
-    tma_load_4d(smem, tmap, bar, gb * tg.GB * kp.gc, wx0, wy0, (int)n);
-  }
-
-  const int per_px = tg.GB * chunks;
-  const int lp = threadIdx.x / per_px, r = threadIdx.x - lp * per_px;
-  const int gl = r / chunks, slice = r - gl * chunks;
-  const int g = gb * tg.GB + gl, c0 = slice * CPT;
-  const int ho = ho0 + lp / kp.tile_w, wo = wo0 + lp % kp.tile_w;
-  const bool active = lp < kp.tile_w * kp.tile_h && ho < kp.Ho && wo < kp.Wo;
-  const bool leader = active && c0 == 0;
-  const uint32_t unit = active ? ((n * (uint32_t)kp.Ho + ho) * kp.Wo + wo) * kp.G + g : 0;
-
-  const T* mrow = mask + (size_t)unit * kp.os_mask;
-  const T* orow = offset + (size_t)unit * kp.os_off;
-  const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
-  const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
-  const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
-  const float ref_y = (float)(ho * kp.stride_h - kp.pad_h + kp.cen_h);
-  const float scale = kp.offset_scale;
-  const int rot = NC > 1 ? lp & (NC - 1) : 0;
-
-  uint32_t gw[NW];
-  if (active) {
-    ldg_words<NW>(gout + (size_t)unit * kp.gc + c0, gw);
-  } else {
-#pragma unroll
-    for (int i = 0; i < NW; ++i) gw[i] = 0u;
-  }
-  rotate_chunks<NW>(gw, rot);
-  Halves<NW> gh;
-  if constexpr (sizeof(T) == 2) gh.split(gw);
-
-  UnitRows<T, KP> rows;
-  bool vec = false;
-  constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
-  if constexpr (kVecRows)
-    vec = active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
-
-  float mx = 0.f, inv = 1.f;
-  if (kp.softmax && active) {
-    mx = -INFINITY;
-    if (vec) {
-#pragma unroll
-      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) mx = fmaxf(mx, rows.msk(p));
-      float s = 0.f;
-#pragma unroll
-      for (int p = 0; p < (KP > 0 ? KP : 1); ++p) s += expf(rows.msk(p) - mx);
-      inv = 1.f / s;
-    } else {
-      for (int p = 0; p < P; ++p) mx = fmaxf(mx, Dt<T>::one(mrow + p));
-      float s = 0.f;
-      for (int p = 0; p < P; ++p) s += expf(Dt<T>::one(mrow + p) - mx);
-      inv = 1.f / s;
-    }
-  }
-
-  // gradient rows: staged after the window, or straight to memory
-  const int lu = threadIdx.x / chunks;
-  const int ub = blockDim.x / chunks;
-  T* ro = la > 0 ? s_rows + lu * la : goff + (size_t)unit * kp.os_off;
-  T* rm = la > 0 ? (kp.merged ? ro + 2 * P : s_rows + ub * la + lu * lb)
-                 : gmask + (size_t)unit * kp.os_mask;
-
-  const bool ready = mbar_wait_bounded(bar, 0, kSplitWaitPolls);
-  if (!ready && threadIdx.x == 0) atomicAdd(&g_split_wait_timeouts, 1ull);
-
-  const uint32_t rb = (uint32_t)(tg.GB * kp.gc) * (uint32_t)sizeof(T);
-  const uint32_t chunk0 = (uint32_t)(gl * kp.gc + c0) * (uint32_t)sizeof(T) / 16u;
-  uint32_t coff[NC];
-#pragma unroll
-  for (int j = 0; j < NC; ++j) coff[j] = 16u * (chunk0 + (uint32_t)((j + rot) & (NC - 1)));
-  const uint32_t sbase = smem_addr(smem);
-
-  float gm_row[KP > 0 ? KP : DCN_MAX_POINTS];
-  float dot = 0.f;
-
-#pragma unroll(KP > 0 ? KP : 1)
-  for (int p = 0; p < P; ++p) {
-    float m = 0.f;
-    float2 d = make_float2(0.f, 0.f);
-    if (KP > 0 && vec) {
-      m = rows.msk(KP > 0 ? p : 0);
-      d = rows.off(KP > 0 ? p : 0);
-    } else if (active) {
-      m = ld_once_1(mrow + p);
-      d = ld_once_2(orow + 2 * p);
-    }
-    if (kp.softmax) m = expf(m - mx) * inv;
-    float x = location(d.x, kp.tap_x[p], scale, ref_x);
-    float y = location(d.y, kp.tap_y[p], scale, ref_y);
-    const bool valid = active && in_box(x, y, kp.W, kp.H);
-    if (!valid) {  // also NaN / inf: the sample contributes nothing
-      x = -4.f;
-      y = -4.f;
-    }
-    const float xf = floorf(x), yf = floorf(y);
-    const int x0 = (int)xf, y0 = (int)yf;
-    const float fx = x - xf, fy = y - yf;
-    const int cx = x0 - wx0, cy = y0 - wy0;
-    float dk[4];
-    if (ready && valid && (unsigned)cx < (unsigned)(tg.WW - 1) &&
-        (unsigned)cy < (unsigned)(tg.WH - 1)) {
-      // in the window: zeros stand for corners outside the image
-      const uint32_t a00 = sbase + (uint32_t)(cy * tg.WW + cx) * rb;
-      const uint32_t at[4] = {a00, a00 + rb, a00 + (uint32_t)tg.WW * rb,
-                              a00 + (uint32_t)tg.WW * rb + rb};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float s2[2] = {0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < NC; ++j) {
-          const uint4 c = lds128(at[k] + coff[j]);
-          const uint32_t cw4[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if constexpr (sizeof(T) == 2) {
-              dot_split<T>(s2[0], s2[1], cw4[e], gh.lo[4 * j + e], gh.hi[4 * j + e]);
-            } else {
-              s2[e & 1] = fmaf(__uint_as_float(gw[4 * j + e]), __uint_as_float(cw4[e]), s2[e & 1]);
-            }
-          }
-        }
-        dk[k] = s2[0] + s2[1];
-      }
-    } else {
-      // far (or invalid: x = y = -4 reads clamped corners that count zero)
-      const bool vx0 = (uint32_t)x0 < W, vx1 = (uint32_t)(x0 + 1) < W;
-      const bool vy0 = (uint32_t)y0 < H, vy1 = (uint32_t)(y0 + 1) < H;
-      const uint32_t xa = min((uint32_t)x0, W - 1), xb = min((uint32_t)(x0 + 1), W - 1);
-      const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
-      const uint32_t off4[4] = {ya * WC + xa * C, ya * WC + xb * C, yb * WC + xa * C,
-                                yb * WC + xb * C};
-      const bool ok[4] = {vy0 && vx0, vy0 && vx1, vy1 && vx0, vy1 && vx1};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t v[NW];
-        ldg_words<NW>(img + off4[k], v);
-        rotate_chunks<NW>(v, rot);
-        float s2[2] = {0.f, 0.f};
-        if constexpr (sizeof(T) == 2) {
-#pragma unroll
-          for (int i = 0; i < NW; ++i) dot_split<T>(s2[0], s2[1], v[i], gh.lo[i], gh.hi[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < NW; ++i)
-            s2[i & 1] = fmaf(__uint_as_float(gw[i]), __uint_as_float(v[i]), s2[i & 1]);
-        }
-        dk[k] = ok[k] && valid ? s2[0] + s2[1] : 0.f;
-      }
-    }
-    for (int s = 1; s < chunks; s <<= 1) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) dk[k] += __shfl_xor_sync(0xffffffffu, dk[k], s);
-    }
-    if (leader) {
-      float gm = 0.f, gox = 0.f, goy = 0.f;
-      if (valid) {
-        const float gx = 1.f - fx, gy = 1.f - fy;
-        gm = gy * (gx * dk[0] + fx * dk[1]) + fy * (gx * dk[2] + fx * dk[3]);
-        gox = scale * m * (gy * (dk[1] - dk[0]) + fy * (dk[3] - dk[2]));
-        goy = scale * m * (gx * (dk[2] - dk[0]) + fx * (dk[3] - dk[1]));
-      }
-      ro[2 * p] = Dt<T>::from_f(gox);
-      ro[2 * p + 1] = Dt<T>::from_f(goy);
-      if (kp.softmax) {
-        gm_row[p] = gm;
-        dot = fmaf(m, gm, dot);
-      } else {
-        rm[p] = Dt<T>::from_f(gm);
-      }
-    }
-  }
-  if (leader && kp.softmax) {
-#pragma unroll(KP > 0 ? KP : 1)
-    for (int p = 0; p < P; ++p) {
-      const float l = KP > 0 && vec ? rows.msk(KP > 0 ? p : 0) : Dt<T>::one(mrow + p);
-      const float m = expf(l - mx) * inv;
-      rm[p] = Dt<T>::from_f(m * (gm_row[p] - dot));
-    }
-  }
-  if (leader && kp.merged)
-    for (int i = 3 * P; i < kp.os_off; ++i) ro[i] = Dt<T>::from_f(0.f);
-  if (la > 0) {
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
-    constexpr int es = (int)sizeof(T);
-    const int nw = min(kp.tile_w, kp.Wo - wo0);
-    for (int tr = warp; tr < kp.tile_h; tr += nwarp) {
-      const int hh = ho0 + tr;
-      if (hh >= kp.Ho) break;
-      const size_t u0 = (((size_t)n * kp.Ho + hh) * kp.Wo + wo0) * kp.G;
-      const int cnt = nw * kp.G, l0 = tr * kp.tile_w * kp.G;
-      warp_copy_out(goff + u0 * kp.os_off, s_rows + l0 * la, cnt * la * es, lane);
-      if (lb > 0)
-        warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * la + l0 * lb, cnt * lb * es, lane);
-    }
-  }
-  // a block whose wait ran out leaves no copy in flight into its memory
-  if (!ready) mbar_wait_bounded(bar, 0, kSplitWaitPolls);
-}
-
 // ---- the input half ---------------------------------------------------------
 // A CTA owns TH x TW <= blockDim.x output pixels of one (image, group); a
 // unit's gc channels are NW words (16, 32 or 64 bytes) and its P <= 16 points.
@@ -900,13 +656,9 @@ bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
 // and shared-memory-bound input blocks side by side instead of one kind after
 // the other.  The two halves share no data: the sample half writes grad_offset
 // and grad_mask, the input half reduces into the cleared accumulator.
-// With kTma the sample blocks stage their input window by a tensor copy
-// (sample_block_tma over the tiles of kp and tg); otherwise they read their
-// corners through L1 (sample_block).
-template <typename T, int CPT, int NW, int KP, bool kTma>
+template <typename T, int CPT, int NW, int KP>
 __global__ void __launch_bounds__(256, 3)
-bwd_both_kernel(const __grid_constant__ CUtensorMap tmap, const TileGeom tg,
-                const KParams kp, const WinGeom wg, const T* __restrict__ gout,
+bwd_both_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
                 const T* __restrict__ input, const T* __restrict__ offset,
                 const T* __restrict__ mask, T* __restrict__ goff, T* __restrict__ gmask, int la,
                 int lb, float* __restrict__ gin, unsigned n_sample, unsigned n_input) {
@@ -920,15 +672,10 @@ bwd_both_kernel(const __grid_constant__ CUtensorMap tmap, const TileGeom tg,
     sample = n_sample > n_input;
     id = b - m;
   }
-  if (sample) {
-    if constexpr (kTma)
-      sample_block_tma<T, CPT, KP>(&tmap, kp, tg, gout, input, offset, mask, goff, gmask, la,
-                                   lb, id);
-    else
-      sample_block<T, CPT, KP>(kp, gout, input, offset, mask, goff, gmask, la, lb, id);
-  } else {
+  if (sample)
+    sample_block<T, CPT, KP>(kp, gout, input, offset, mask, goff, gmask, la, lb, id);
+  else
     input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, id);
-  }
 }
 
 
@@ -988,43 +735,32 @@ static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T*
 template <typename T, int CPT, int NW>
 static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* go_, const T* i_,
                                  const T* o_, const T* m_, T* goff_, T* gm_, int la, int lb,
-                                 float* acc, const void* map, const TileGeom* tg,
-                                 cudaStream_t s) {
+                                 float* acc, cudaStream_t s) {
   const int chunks = kp.gc / CPT;
   const int block = 256;
-  const long long na = map ? (long long)kp.N * kp.tiles_w * kp.tiles_h * tg->ngb
-                           : kp.tile_w > 0 ? (long long)kp.N * kp.tiles_w * kp.tiles_h
-                                           : (kp.units * chunks + block - 1) / block;
+  const long long na = kp.tile_w > 0 ? (long long)kp.N * kp.tiles_w * kp.tiles_h
+                                     : (kp.units * chunks + block - 1) / block;
   const long long nb = (long long)kp.N * kp.G * wg.tiles_h * wg.tiles_w;
   if (na + nb > INT_MAX) return cudaErrorInvalidConfiguration;
-  const size_t sa = (map ? tg->win_bytes + 16 : 0) +
-                    (la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0);
+  const size_t sa = la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0;
   const size_t sb = split_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
   const size_t smem = sa > sb ? sa : sb;
-  auto k = map ? (kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9, true>
-                            : kp.P == 8 ? bwd_both_kernel<T, CPT, NW, 8, true>
-                                        : bwd_both_kernel<T, CPT, NW, 0, true>)
-               : (kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9, false>
-                            : kp.P == 8 ? bwd_both_kernel<T, CPT, NW, 8, false>
-                                        : bwd_both_kernel<T, CPT, NW, 0, false>);
+  auto k = kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9>
+         : kp.P == 8 ? bwd_both_kernel<T, CPT, NW, 8>
+                     : bwd_both_kernel<T, CPT, NW, 0>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  CUtensorMap none;
-  std::memset(&none, 0, sizeof none);
-  const TileGeom tg0 = tg ? *tg : TileGeom{};
-  k<<<(unsigned)(na + nb), block, smem, s>>>(
-      map ? *static_cast<const CUtensorMap*>(map) : none, tg0, kp, wg, go_, i_, o_, m_, goff_,
-      gm_, la, lb, acc, (unsigned)na, (unsigned)nb);
+  k<<<(unsigned)(na + nb), block, smem, s>>>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc,
+                                             (unsigned)na, (unsigned)nb);
   return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, int la, int lb,
                                 const void* gout, const void* in, const void* off, const void* msk,
-                                float* acc, void* gin, void* goff, void* gmask, const void* map,
-                                const TileGeom* tg, cudaStream_t s) {
+                                float* acc, void* gin, void* goff, void* gmask, cudaStream_t s) {
   const T* go_ = static_cast<const T*>(gout);
   const T* i_ = static_cast<const T*>(in);
   const T* o_ = static_cast<const T*>(off);
@@ -1037,20 +773,20 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
     // the (channels per sample thread, words per unit row) pairs that occur
     if constexpr (sizeof(T) == 2) {
       if (cpt == 8 && nw == 4)
-        e = launch_both_t<T, 8, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 8, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else if (cpt == 16 && nw == 8)
-        e = launch_both_t<T, 16, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 16, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else if (cpt == 16 && nw == 16)
-        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else
         return cudaErrorInvalidValue;
     } else {
       if (cpt == 4 && nw == 4)
-        e = launch_both_t<T, 4, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 4, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else if (cpt == 8 && nw == 8)
-        e = launch_both_t<T, 8, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 8, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else if (cpt == 16 && nw == 16)
-        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, map, tg, s);
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
       else
         return cudaErrorInvalidValue;
     }
@@ -1085,23 +821,19 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
 cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, int cpt, int la,
                              int lb, const void* gout, const void* in, const void* off,
                              const void* msk, float* gin_acc, void* gin, void* goff, void* gmask,
-                             const void* map, const TileGeom* tg, cudaStream_t s) {
+                             cudaStream_t s) {
   switch (dtype) {
     case DCN_F32:
       return launch_split<float>(kp, wg, cpt, la, lb, gout, in, off, msk, gin_acc, gin, goff,
-                                 gmask, map, tg, s);
+                                 gmask, s);
     case DCN_F16:
       return launch_split<__half>(kp, wg, cpt, la, lb, gout, in, off, msk, gin_acc, gin, goff,
-                                  gmask, map, tg, s);
+                                  gmask, s);
     case DCN_BF16:
       return launch_split<__nv_bfloat16>(kp, wg, cpt, la, lb, gout, in, off, msk, gin_acc, gin,
-                                         goff, gmask, map, tg, s);
+                                         goff, gmask, s);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t read_split_wait_timeouts(unsigned long long* count) {
-  return cudaMemcpyFromSymbol(count, g_split_wait_timeouts, sizeof(unsigned long long));
 }
 
 }  // namespace dcn

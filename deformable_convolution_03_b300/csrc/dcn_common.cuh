@@ -54,9 +54,9 @@ struct KParams {
   float tap_y[DCN_MAX_POINTS];
 };
 
-// Geometry of the windowed backward (bwd_window_kernel): a CTA owns TH x TW
-// output pixels of one (image, group) and a window of WH x WW input pixels
-// whose origin, for the tile starting at output (ho0, wo0), is
+// Geometry of the split backward's input blocks (dcn_bwd_split.cu): a CTA owns TH
+// x TW output pixels of one (image, group) and a window of WH x WW input
+// pixels whose origin, for the tile starting at output (ho0, wo0), is
 // (ho0*stride_h + org_y, wo0*stride_w + org_x).
 struct WinGeom {
   int TH, TW;
@@ -76,15 +76,6 @@ struct TileGeom {
   int org_y, org_x;
   unsigned win_bytes;
 };
-
-// Shared memory of bwd_window_kernel: TH*TW*P sample entries in cell order
-// (16 B each), the tile's grad_out (gc*es bytes per output pixel), and
-// per-cell counts, list heads and cursors ((WH-1)*(WW-1) cells).
-__host__ __device__ inline size_t window_smem_bytes(const WinGeom& wg, int P, int gc, int es) {
-  const size_t nunit = (size_t)wg.TH * wg.TW, nsamp = nunit * P;
-  const size_t ncell = (size_t)(wg.WH - 1) * (wg.WW - 1);
-  return nsamp * 16 + nunit * gc * es + (3 * ncell + 1) * sizeof(int);
-}
 
 // Shared memory of bwd_input_kernel: per sample (TH*TW*P), in cell order, its
 // four corner weights (4 x 16 bits for 16-bit storage, 4 x float32 otherwise)

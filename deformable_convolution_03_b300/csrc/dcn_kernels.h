@@ -26,14 +26,6 @@ cudaError_t launch_bwd(const KParams& kp, int dtype, int cpt, const void* gout, 
 // float32 accumulator -> 16-bit grad_input (n elements), rounding to nearest.
 cudaError_t launch_round(int dtype, const float* acc, void* out, long long n, cudaStream_t s);
 
-// The windowed backward (dcn_bwd_window.cu): cpt 4, 8 or 16 with cpt*sizeof(T)
-// of 16 to 64 bytes, gc/cpt a power of two no larger than 32, P <= 16; 256
-// threads per CTA = TH*TW*(gc/cpt).  gin_acc (float32) must be cleared by the
-// caller; when it is not gin, it is rounded into gin at the end.
-cudaError_t launch_bwd_window(const KParams& kp, const WinGeom& wg, int dtype, int cpt,
-                              const void* gout, const void* in, const void* off, const void* msk,
-                              float* gin_acc, void* gin, void* goff, void* gmask, cudaStream_t s);
-
 // The split backward (dcn_bwd_split.cu): bwd_sample_kernel (grad_offset,
 // grad_mask) with cpt as the wide forward's and the tiles in kp, then
 // bwd_input_kernel (grad_input) over the windows of wg, gc*sizeof(T) of 16,
@@ -41,14 +33,10 @@ cudaError_t launch_bwd_window(const KParams& kp, const WinGeom& wg, int dtype, i
 // staged offset and mask rows (0: written straight to memory).  gin_acc
 // (float32) must be cleared by the caller; when it is not gin, it is rounded
 // into gin at the end.
-// map / tg: when map is not NULL, the sample blocks of the fused launch
-// stage their input windows with that tensor map over the tiles of kp and tg
-// (see encode_input_map); otherwise they read through L1 over kp's tiles.
 cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, int cpt, int la,
                              int lb, const void* gout, const void* in, const void* off,
                              const void* msk, float* gin_acc, void* gin, void* goff, void* gmask,
-                             const void* map, const TileGeom* tg, cudaStream_t s);
-cudaError_t read_split_wait_timeouts(unsigned long long* count);
+                             cudaStream_t s);
 
 // The TMA-staged forward (dcn_fwd_tma.cu).  encode_input_map fills the
 // 128-byte tensor map of the input (dims C, W, H, N; box GB*gc x WW x WH x 1;

@@ -21,11 +21,8 @@ struct Options {
   // backward
   int bwd_split = 2;      // 2: split kernels for 16-bit storage, 1: for any dtype, 0: never
   int bwd_fuse = 1;       // both split halves in one launch
-  int bwd_tma = 0;        // split sample blocks with TMA-staged windows
-  int bwd_tma_kb = 40;    // their window budget (KB)
-  int bwd_window = 2;     // 2: the window kernel for strides >= 2, 1: always, 0: never
   int bwd_cpt = 4;        // largest slice of the single-pass kernel
-  int bwd_halo = 6;       // halo (pixels) of the split / window kernels' windows
+  int bwd_halo = 6;       // halo (pixels) of the split input blocks' windows
   int bwd_stage = 1;      // gradient rows staged in shared memory
   // projections
   int linear_tc = 1;       // tensor-core kernels where they apply

@@ -31,8 +31,7 @@ CASES = [
 BWD = {
     "default": {},
     "split": {"bwd_split": 1},
-    "split_tma": {"bwd_split": 1, "bwd_tma": 1},
-    "single_pass": {"bwd_split": 0, "bwd_window": 0},
+    "single_pass": {"bwd_split": 0},
 }
 
 

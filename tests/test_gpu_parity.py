@@ -107,7 +107,7 @@ def test_small_forward_and_backward(w):
 @pytest.mark.parametrize("cap", [1, 2, 4, 8, 16, 32])
 def test_every_general_kernel_instance(dt, cap, opts):
     # force each channels-per-thread instance of the general kernels
-    opts.update({"fwd_wide": 0, "bwd_split": 0, "bwd_window": 0,
+    opts.update({"fwd_wide": 0, "bwd_split": 0,
                  "fwd_cpt": cap, "bwd_cpt": cap})
     w = small(f"inst_{dt}_{cap}", dt, gc=32, G=2, softmax=1, N=3, H=10, W=9)
     t = make_inputs(w)
@@ -194,15 +194,8 @@ BWD_MODES = {
     "split_direct": {"bwd_split": 1, "bwd_stage": 0, "fwd_tile": 0},
     # the two split kernels as separate launches instead of one
     "split_unfused": {"bwd_split": 1, "bwd_fuse": 0},
-    # the fused launch with the sample blocks' input windows staged by a
-    # tensor copy, with a small window (many far samples)
-    "split_tma": {"bwd_split": 1, "bwd_tma": 1},
-    "split_tma_small": {"bwd_split": 1, "bwd_tma": 1, "bwd_tma_kb": 8},
-    # the fused windowed kernel, with its default halo and with one pixel
-    "window": {"bwd_split": 0, "bwd_window": 1},
-    "window_halo1": {"bwd_split": 0, "bwd_window": 1, "bwd_halo": 1},
     # the single-pass atomic kernels
-    "single_pass": {"bwd_split": 0, "bwd_window": 0},
+    "single_pass": {"bwd_split": 0},
 }
 
 
@@ -214,7 +207,7 @@ def test_backward_paths(w, mode, opts):
 
 
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
-@pytest.mark.parametrize("mode", ["split", "window", "single_pass"])
+@pytest.mark.parametrize("mode", ["split", "single_pass"])
 def test_backward_crowded_samples(dt, mode, opts):
     # every sample of a 32x32 image aimed at one cell: the cells inside each
     # tile's window collect hundreds of samples, the rest leave the window
