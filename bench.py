@@ -20,8 +20,9 @@ storage), on seeded synthetic inputs already resident in HBM.
   cpu_baseline = the oracle (plain binary64 loops) on the host cores, on a
               bounded sample of the same workload
   projections = the layers around the core at the workload's shape, beside
-              the step: the offset/mask and output projections (dcn_linear) and
-              the centre feature scale (forward and backward)
+              the step: the offset/mask and output projections (dcn_linear),
+              the centre feature scale (forward and backward) and the offset
+              branch's feature step (dcn_dwconv_ln_gelu, 5 x 5)
 
 L2 is flushed (a write of twice its size) before every timed step, outside
 the step's events.  ``--impl reference`` times the oracle alone, on the host.
@@ -47,7 +48,11 @@ from deformable_convolution_03_b300 import binding as B  # noqa: E402
 from deformable_convolution_03_b300.replicas import (  # noqa: E402
     aggregate_gbs, max_over_ranks, rank_seed)
 from deformable_convolution_03_b300.inputs import (  # noqa: E402
-    DTYPES, T_DEPTHS, WORKLOADS, Workload, ideal_bytes, make_inputs)
+    DTYPES, T_DEPTHS, WORKLOADS, Workload, ideal_bytes, make_dwconv_inputs, make_inputs)
+
+# The depthwise kernel of the offset branch's feature step (dw_kernel_size 5,
+# page "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 一).
+DW_KERNEL = 5
 
 METRIC = "DCN core fwd/bwd GB/s and % of HBM roofline; images/s at FlashInternImage-T shapes"
 UNIT = "GB/s"
@@ -377,18 +382,7 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
         x = (torch.rand(M, C, generator=g) * 2 - 1).to(dt).to(dev)
         wt = (torch.randn(n_out, C, generator=g) / C ** 0.5).to(dt).to(dev)
         b = torch.randn(n_out, generator=g).to(dt).to(dev)
-        for _ in range(3):
-            B.linear(x, wt, b)
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            B.linear(x, wt, b)
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        ms = statistics.mean(ts)
+        ms = _time_alone(lambda: B.linear(x, wt, b), flush, reps)
         es = torch.empty(0, dtype=dt).element_size()
         ideal = (M * C + n_out * C + n_out + M * n_out) * es
         gbs = ideal / (ms * 1e-3) / 1e9
@@ -406,22 +400,39 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
                          (5 * M * C + 2 * M * w.G) * es),
     }
     for name, (fn, ideal) in gates.items():
-        for _ in range(3):
-            fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        ms = statistics.mean(ts)
+        ms = _time_alone(fn, flush, reps)
         gbs = ideal / (ms * 1e-3) / 1e9
         out[name] = {"shape": f"{M}x{C}, {w.G} gates", "ms": round(ms, 5), "GB/s": round(gbs, 1),
                      "frac_hbm": round(gbs / peak, 4), "ideal_bytes": ideal}
+    # the offset branch's feature step on the core's input: 5 x 5 depthwise
+    # convolution, LayerNorm and GELU in one pass (x read once, x1 written once)
+    t = make_dwconv_inputs(w.N, w.H, w.W, C, DW_KERNEL, w.dtype, seed=78)
+    t = {key: v.to(dev) for key, v in t.items()}
+    ideal = (2 * w.N * w.H * w.W * C + (DW_KERNEL ** 2 + 3) * C) * es
+    ms = _time_alone(lambda: B.dwconv_ln_gelu(t["x"], t["weight"], t["bias"], t["gamma"],
+                                              t["beta"]), flush, reps)
+    gbs = ideal / (ms * 1e-3) / 1e9
+    out["dwconv_ln_gelu"] = {"shape": f"{w.N}x{w.H}x{w.W}x{C}, k{DW_KERNEL}", "ms": round(ms, 5),
+                             "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
+                             "ideal_bytes": ideal}
     return out
+
+
+def _time_alone(fn, flush, reps: int) -> float:
+    """Mean ms of fn over reps calls, each after an L2 flush, by CUDA events on
+    the current stream (three untimed calls first)."""
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.mean(ts)
 
 
 def images_per_s(dev, flush, reps: int):
@@ -547,7 +558,10 @@ def profile_proj(dev) -> int:
     FlashInternImage-T stage 1's merged offset/mask projection (200704 x 64 ->
     128) and output projection (-> 64) in float16, InternImage-G stage 1's
     512 -> 512 projection (32768 rows) in bfloat16, and the centre feature
-    scale forward and backward at stage 1 (200704 x 64, 4 gates, float16)."""
+    scale forward and backward at stage 1 (200704 x 64, 4 gates, float16), and
+    the offset branch's feature step (5 x 5 depthwise convolution, LayerNorm,
+    GELU) at T stage 1 (64 x 56 x 56 x 64, float16) and G stage 1
+    (2 x 128 x 128 x 512, bfloat16)."""
     g = torch.Generator().manual_seed(1)
     calls = []
     for M, K, N, dt in ((200704, 64, 128, torch.float16), (200704, 64, 64, torch.float16),
@@ -561,6 +575,11 @@ def profile_proj(dev) -> int:
     lg = torch.randn(M, G, generator=g).half().to(dev)
     calls.append(lambda: B.center_feature_scale(core, xp, lg))
     calls.append(lambda: B.center_feature_scale_backward(go, core, xp, lg))
+    for N, H, C, dt in ((64, 56, 64, "f16"), (2, 128, 512, "bf16")):
+        t = {key: v.to(dev) for key, v in
+             make_dwconv_inputs(N, H, H, C, DW_KERNEL, dt, seed=2).items()}
+        calls.append(lambda t=t: B.dwconv_ln_gelu(t["x"], t["weight"], t["bias"], t["gamma"],
+                                                  t["beta"]))
     for f in calls:
         f()
         f()

@@ -8,4 +8,4 @@ from .binding import (  # noqa: F401
     DCN_BF16, DCN_F16, DCN_F32, DCNError, Params, center_feature_scale,
     center_feature_scale_backward, core_bwd, core_fwd, dcn_core, dcn_core_bwd,
     dcn_core_bwd_workspace, dcn_core_fwd, dcn_num_points, dcn_out_shape, dcn_status_str,
-    dcn_version, linear)
+    dcn_version, dwconv_ln_gelu, linear)

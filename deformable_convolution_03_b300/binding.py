@@ -33,8 +33,10 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
            "dcn_linear", "dcn_center_feature_scale", "dcn_center_feature_scale_bwd",
-           "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
+           "dcn_dwconv_ln_gelu", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
+DCN_DW_MAX_KERNEL = 31
+DCN_DW_MAX_CHANNELS = 2048
 
 
 class DCNError(RuntimeError):
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
         L.dcn_center_feature_scale.argtypes = [ctypes.POINTER(dcn_cfs_params_t), vp, vp, vp, vp,
                                                vp]
         L.dcn_center_feature_scale_bwd.argtypes = [ctypes.POINTER(dcn_cfs_params_t)] + [vp] * 8
+        L.dcn_dwconv_ln_gelu.argtypes = [ctypes.POINTER(dcn_dwconv_params_t)] + [vp] * 7
         L.dcn_status_str.argtypes = [ctypes.c_int]
         L.dcn_status_str.restype = ctypes.c_char_p
         _lib = L
@@ -225,6 +228,43 @@ def center_feature_scale_backward(grad_out, core, x_proj, logits):
                                  gx.reshape(-1, C), gl.reshape(-1, G), G,
                                  torch.cuda.current_stream(core.device).cuda_stream)
     return gc, gx, gl
+
+
+class dcn_dwconv_params_t(ctypes.Structure):
+    """Mirror of dcn_dwconv_params_t (include/dcn_core.h)."""
+    _fields_ = [("N", ctypes.c_int), ("H", ctypes.c_int), ("W", ctypes.c_int),
+                ("C", ctypes.c_int), ("k", ctypes.c_int), ("eps", ctypes.c_float),
+                ("dtype", ctypes.c_int)]
+
+
+def dcn_dwconv_ln_gelu(x, weight, bias, gamma, beta, y, eps: float, stream=None) -> None:
+    """Raw entry point: y = GELU(LayerNorm(depthwise k x k conv of x + bias));
+    x, y (N, H, W, C), weight (k, k, C), bias (C) or None, gamma, beta (C)."""
+    N, H, W, C = (int(v) for v in x.shape)
+    p = dcn_dwconv_params_t(N, H, W, C, int(weight.shape[0]), float(eps), TORCH_TO_DCN[x.dtype])
+    _check(lib().dcn_dwconv_ln_gelu(ctypes.byref(p), _ptr(x), _ptr(weight), _ptr(bias),
+                                    _ptr(gamma), _ptr(beta), _ptr(y), _stream(stream)),
+           "dcn_dwconv_ln_gelu")
+
+
+def dwconv_ln_gelu(x, weight, bias, gamma, beta, eps: float = 1e-6):
+    """The offset branch's feature step on the GPU: x (N, H, W, C) channels-last,
+    weight (k, k, C) (a depthwise Conv2d weight (C, 1, k, k) permuted to
+    (k, k, C)), bias (C) or None, gamma, beta (C); returns a new (N, H, W, C)."""
+    ts = (x, weight, gamma, beta) + ((bias,) if bias is not None else ())
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != x.dtype:
+            raise ValueError("dwconv_ln_gelu: contiguous CUDA tensors of one dtype expected")
+    if x.dim() != 4:
+        raise ValueError(f"dwconv_ln_gelu: x must be (N, H, W, C), got {tuple(x.shape)}")
+    C, k = x.shape[3], weight.shape[0]
+    if weight.shape != (k, k, C) or gamma.shape != (C,) or beta.shape != (C,) or (
+            bias is not None and bias.shape != (C,)):
+        raise ValueError("dwconv_ln_gelu: parameter shapes do not match the channels")
+    y = torch.empty_like(x)
+    dcn_dwconv_ln_gelu(x, weight, bias, gamma, beta, y, eps,
+                       torch.cuda.current_stream(x.device).cuda_stream)
+    return y
 
 
 def dcn_wait_timeouts() -> int:

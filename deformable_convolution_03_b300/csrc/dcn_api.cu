@@ -385,7 +385,14 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
   return cpt;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCN_OK : DCN_ERR_CUDA; }
+// The CUDA error behind this thread's last DCN_ERR_CUDA (a test hook reads it).
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DCN_OK;
+  g_last_cuda_error = (int)e;
+  return DCN_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -556,6 +563,66 @@ int cfs_check(const dcn_cfs_params_t* p, int* es) {
 
 }  // namespace
 
+namespace {
+
+// Shared memory the tiled feature-step kernel takes per block: within
+// kDwSmemTwo two blocks fit on an SM; up to kDwSmemOne, one.
+constexpr size_t kDwSmemTwo = 110 * 1024;
+constexpr size_t kDwSmemOne = 220 * 1024;
+
+// Validates a feature-step call and picks its kernel: the tiled one when the
+// shape and the alignments allow, with about 128 threads a block (patches
+// from C; a 512-channel patch takes 256), 4-row patches unless only 2-row
+// ones let two blocks share an SM, and as many patches as then fit; else the
+// one-warp-per-pixel kernel.
+int dwconv_plan(const dcn_dwconv_params_t* p, const void* x, const void* w, const void* b,
+                const void* g, const void* bt, const void* y, dcn::DwGeom* d) {
+  if (!p) return DCN_ERR_NULL;
+  const int es = elem_size(p->dtype);
+  if (es == 0) return DCN_ERR_DTYPE;
+  if (p->N < 0 || p->H < 1 || p->W < 1 || p->C < 1 || p->k < 1 || p->k % 2 == 0 ||
+      p->k > DCN_DW_MAX_KERNEL || !(p->eps >= 0.f) || !std::isfinite(p->eps))
+    return DCN_ERR_SHAPE;
+  if (p->C > DCN_DW_MAX_CHANNELS) return DCN_ERR_UNSUPPORTED;
+  const long long hw = (long long)p->H * p->W;
+  if (p->H > kMaxExtent || p->W > kMaxExtent || (long long)p->N * hw > (1LL << 40) / p->C)
+    return DCN_ERR_UNSUPPORTED;
+  *d = dcn::DwGeom{p->N, p->H, p->W, p->C, p->k, p->eps, false, 1, 1, 4};
+  if ((long long)p->N * hw == 0) return DCN_OK;
+  if (!x || !w || !g || !bt || !y) return DCN_ERR_NULL;
+  for (const void* q : {x, w, g, bt, y})
+    if (!aligned(q, es)) return DCN_ERR_ALIGN;
+  if (b && !aligned(b, es)) return DCN_ERR_ALIGN;
+  const dcn::Options& o = dcn::options();
+  bool tiled = o.dw_tiled && (p->k == 3 || p->k == 5) &&
+               (p->C == 64 || p->C == 128 || p->C == 256 || p->C == 512) && aligned(x, 16);
+  for (const void* q : {w, b, g, bt, y}) tiled = tiled && (!q || aligned(q, 2 * es));
+  if (tiled) {
+    int np0 = std::max(1, 128 / (p->C / 2));  // 128 threads measured faster than 256
+    if (o.dw_patches > 0) np0 = std::min(o.dw_patches, std::max(1, 256 / (p->C / 2)));
+    np0 = 1 << (31 - __builtin_clz((unsigned)np0));  // a power of two
+    // 4-row patches first (fewer footprint reads per output), then 2-row
+    for (const size_t cap : {kDwSmemTwo, kDwSmemOne}) {
+      for (const int py : {4, 2}) {
+        if (o.dw_py && py != o.dw_py) continue;
+        for (int np = np0; np >= 1 && !d->tiled; np /= 2) {
+          d->ph = np >= 4 ? 2 : 1;
+          d->pw = np / d->ph;
+          d->py = py;
+          d->tiled = true;  // dwconv_smem_bytes sizes the tiled kernel's buffers
+          d->tiled = dcn::dwconv_smem_bytes(*d, es) <= cap;
+        }
+        if (d->tiled) break;
+      }
+      if (d->tiled) break;
+    }
+  }
+  if (!d->tiled) d->ph = d->pw = 1, d->py = 4;
+  return DCN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int dcn_core_bwd(const dcn_params_t* p, const void* grad_out, const void* input,
@@ -660,6 +727,17 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
                                          static_cast<cudaStream_t>(stream)));
 }
 
+int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* weight,
+                       const void* bias, const void* gamma, const void* beta, void* y,
+                       void* stream) {
+  dcn::DwGeom d{};
+  if (const int rc = dwconv_plan(p, x, weight, bias, gamma, beta, y, &d)) return rc;
+  if ((long long)p->N * p->H * p->W == 0) return DCN_OK;
+  if (fault_injected()) return DCN_ERR_CUDA;
+  return cuda_status(dcn::launch_dwconv(d, p->dtype, x, weight, bias, gamma, beta, y,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 // ---- the selection switches and their test hook ----------------------------
@@ -696,6 +774,9 @@ constexpr OptionName kOptionNames[] = {
     {"linear_s", &dcn::Options::linear_s},
     {"linear_ctas", &dcn::Options::linear_ctas},
     {"linear_persist", &dcn::Options::linear_persist},
+    {"dw_tiled", &dcn::Options::dw_tiled},
+    {"dw_patches", &dcn::Options::dw_patches},
+    {"dw_py", &dcn::Options::dw_py},
     {"fault_inject", &dcn::Options::fault_inject},
 };
 }  // namespace
@@ -714,3 +795,7 @@ extern "C" int dcn_internal_set_option(const char* name, int value) {
 }
 
 extern "C" void dcn_internal_reset_options(void) { dcn::g_options = dcn::Options(); }
+
+// Test hook: the cudaError_t behind the calling thread's last DCN_ERR_CUDA
+// from a CUDA call (0 if none).
+extern "C" int dcn_internal_last_cuda_error(void) { return g_last_cuda_error; }

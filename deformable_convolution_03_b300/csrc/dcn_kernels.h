@@ -70,4 +70,19 @@ cudaError_t launch_cfs_bwd(int dtype, int vbytes, long long M, int C, int G, con
                            const void* core, const void* x, const void* logits, void* gcore,
                            void* gx, void* glogits, cudaStream_t s);
 
+// The offset branch's feature step (dcn_dwconv.cu).  tiled: the tiled kernel
+// (k of 3 or 5, C of 64, 128, 256 or 512, the input 16-byte aligned and
+// every other tensor aligned to two elements) with ph x pw patches of py x 4
+// pixels per block (py of 2 or 4; ph * pw * C / 2 threads, at most 256);
+// otherwise the one-warp-per-pixel kernel (C up to 2048).
+struct DwGeom {
+  int N, H, W, C, k;
+  float eps;
+  bool tiled;
+  int ph, pw, py;
+};
+size_t dwconv_smem_bytes(const DwGeom& d, int es);
+cudaError_t launch_dwconv(const DwGeom& d, int dtype, const void* x, const void* w, const void* b,
+                          const void* g, const void* bt, void* y, cudaStream_t s);
+
 }  // namespace dcn

@@ -31,6 +31,10 @@ struct Options {
   int linear_s = 8;        // its largest stage count
   int linear_ctas = 2;     // persistent CTAs per SM when they fit
   int linear_persist = 1;  // the persistent kernel where it applies
+  // the offset branch's feature step
+  int dw_tiled = 1;      // the tiled kernel where it applies
+  int dw_patches = 0;    // patches of a tiled block, at most 256 threads (0: about 128 threads)
+  int dw_py = 0;         // patch rows of the tiled kernel (2 or 4; 0: from the shared memory)
   // a valid call reports DCN_ERR_CUDA before any CUDA call (error-path tests)
   int fault_inject = 0;
 };

@@ -146,6 +146,26 @@ def make_inputs(w: Workload, seed: int | None = None, grad: bool | None = None) 
     return out
 
 
+def make_dwconv_inputs(N: int, H: int, W: int, C: int, k: int, dtype: str, seed: int = 0,
+                       bias: bool = True) -> dict:
+    """Seeded CPU tensors for the offset branch's feature step, in the storage
+    dtype: x (N,H,W,C) U(-1, 1) like the core's input; the depthwise kernel
+    (k,k,C) and bias (C) U(-1/k, 1/k) (a convolution layer's default
+    initialisation, fan-in k*k); LayerNorm gamma 1 + N(0, 0.1) and beta
+    N(0, 0.1) (its default 1 and 0, perturbed so that both matter)."""
+    dt = DTYPES[dtype]
+
+    def gen(j: int) -> torch.Generator:
+        return torch.Generator().manual_seed(seed * 16 + 8 + j)
+
+    out = {"x": (torch.rand((N, H, W, C), generator=gen(0)) * 2 - 1).to(dt),
+           "weight": ((torch.rand((k, k, C), generator=gen(1)) * 2 - 1) / k).to(dt),
+           "gamma": (1 + 0.1 * torch.randn(C, generator=gen(3))).to(dt),
+           "beta": (0.1 * torch.randn(C, generator=gen(4))).to(dt)}
+    out["bias"] = ((torch.rand(C, generator=gen(2)) * 2 - 1) / k).to(dt) if bias else None
+    return out
+
+
 def ideal_bytes(w: Workload) -> dict:
     """Bytes that must cross HBM at least once: each tensor read or written once.
 

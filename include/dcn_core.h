@@ -258,6 +258,51 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
                                  void* grad_core, void* grad_x_proj, void* grad_logits,
                                  void* stream);
 
+/* The feature step of the DCN module's offset branch (page
+ * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
+ * item 2: the control features x1 from which the offset and mask projections
+ * are computed come from a depthwise convolution, LayerNorm and GELU of the
+ * module's input; the page's configuration table gives dw_kernel_size 5).
+ * One pass computes, per image n, pixel (i, j) and channel c,
+ *     u[c] = bias[c] + sum_{a,e < k} weight[a, e, c] * x[n, i+a-r, j+e-r, c]
+ *            (r = (k - 1) / 2, x zero outside the image: the output keeps the
+ *            input's size),
+ *     z[c] = (u[c] - mean(u)) / sqrt(var(u) + eps) * gamma[c] + beta[c]
+ *            (mean and biased variance over the pixel's C channels),
+ *     y[n, i, j, c] = z / 2 * (1 + erf(z / sqrt(2)))   (the exact GELU).
+ *   x       (N, H, W, C) channels-last, read
+ *   weight  (k, k, C)    the depthwise kernel, weight[a, e, c] = a PyTorch
+ *                        Conv2d(groups=C) weight[c, 0, a, e], read
+ *   bias    (C) or NULL (no bias), read
+ *   gamma, beta (C)      the LayerNorm affine parameters, read
+ *   y       (N, H, W, C) fully overwritten; must not overlap x
+ * One dtype for all.  Arithmetic in float32 (the convolution's k*k products
+ * summed in float32, the statistics over float32 sums), one rounding to the
+ * storage type; erf is evaluated by Abramowitz and Stegun's formula 7.1.26
+ * (absolute error at most 1.5e-7), so GELU is within |z| * 1e-7 of exact
+ * before rounding.  The library picks a tiled kernel for k of 3 or 5 with C
+ * of 64, 128, 256 or 512, x 16-byte aligned and the other tensors aligned
+ * to two elements; any other shape within the limits takes a slower kernel
+ * with the same arithmetic.  N == 0 launches nothing.
+ * DCN_ERR_NULL / DCN_ERR_DTYPE / DCN_ERR_SHAPE (N < 0, H < 1, W < 1, C < 1,
+ * k even, k < 1 or k > DCN_DW_MAX_KERNEL, eps negative or not finite) /
+ * DCN_ERR_ALIGN (a pointer not aligned to the element size) /
+ * DCN_ERR_UNSUPPORTED (C > DCN_DW_MAX_CHANNELS, N * H * W * C >= 2^40) before
+ * any CUDA call. */
+#define DCN_DW_MAX_KERNEL 31
+#define DCN_DW_MAX_CHANNELS 2048
+
+typedef struct {
+  int N, H, W, C;  /* images, height, width, channels */
+  int k;           /* kernel size (odd) */
+  float eps;       /* LayerNorm epsilon */
+  int dtype;       /* dcn_dtype_t of every tensor */
+} dcn_dwconv_params_t;
+
+int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* weight,
+                       const void* bias, const void* gamma, const void* beta, void* y,
+                       void* stream);
+
 /* Diagnostics of the asynchronous tensor copies some kernels use: the number
  * of thread blocks, since the library was loaded, whose bounded wait for such a
  * copy ran out on the current device.  Such a block computed its results from

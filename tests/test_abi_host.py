@@ -252,3 +252,46 @@ def test_centre_feature_scale_argument_errors(native):
     p0 = ctypes.byref(_cfs(native, 0, 64, 4))
     assert f(p0, None, None, None, None, None) == native.DCN_OK
     assert b(p0, *([None] * 7), None) == native.DCN_OK
+
+
+# ---- the offset branch's feature step: argument errors before any CUDA call --
+
+def _dw(native, N, H, W, C, k, eps=1e-6, dtype=None):
+    return native.dcn_dwconv_params_t(N, H, W, C, k, eps,
+                                      native.DCN_BF16 if dtype is None else dtype)
+
+
+@host_only
+def test_dwconv_argument_errors(native, opts):
+    L = native.lib()
+    g = 0x10000
+    f = L.dcn_dwconv_ln_gelu
+    assert f(None, g, g, g, g, g, g, None) == native.DCN_ERR_NULL
+    assert f(ctypes.byref(_dw(native, 1, 8, 8, 64, 5, dtype=7)), g, g, g, g, g, g,
+             None) == native.DCN_ERR_DTYPE
+    for N, H, W, C, k, eps in ((-1, 8, 8, 64, 5, 1e-6), (1, 0, 8, 64, 5, 1e-6),
+                               (1, 8, 0, 64, 5, 1e-6), (1, 8, 8, 0, 5, 1e-6),
+                               (1, 8, 8, 64, 4, 1e-6), (1, 8, 8, 64, 0, 1e-6),
+                               (1, 8, 8, 64, native.DCN_DW_MAX_KERNEL + 2, 1e-6),
+                               (1, 8, 8, 64, 5, -1e-6), (1, 8, 8, 64, 5, float("nan")),
+                               (1, 8, 8, 64, 5, float("inf"))):
+        assert f(ctypes.byref(_dw(native, N, H, W, C, k, eps)), g, g, g, g, g, g,
+                 None) == native.DCN_ERR_SHAPE, (N, H, W, C, k, eps)
+    assert f(ctypes.byref(_dw(native, 1, 8, 8, native.DCN_DW_MAX_CHANNELS + 64, 5)), g, g, g, g,
+             g, g, None) == native.DCN_ERR_UNSUPPORTED
+    assert f(ctypes.byref(_dw(native, 1 << 20, 1 << 10, 1 << 10, 64, 5)), g, g, g, g, g, g,
+             None) == native.DCN_ERR_UNSUPPORTED
+    p = ctypes.byref(_dw(native, 2, 8, 8, 64, 5))
+    for i in (0, 1, 3, 4, 5):  # x, weight, gamma, beta, y; the bias may be NULL
+        args = [g] * 6
+        args[i] = None
+        assert f(p, *args, None) == native.DCN_ERR_NULL, i
+        args[i] = g + 1
+        assert f(p, *args, None) == native.DCN_ERR_ALIGN, i
+    assert f(p, g, g, g + 1, g, g, g, None) == native.DCN_ERR_ALIGN
+    # no images: nothing to do, and nothing is touched
+    p0 = ctypes.byref(_dw(native, 0, 8, 8, 64, 5))
+    assert f(p0, None, None, None, None, None, None, None) == native.DCN_OK
+    # a valid call stops at the fault hook, before any CUDA call
+    opts.set("fault_inject", 1)
+    assert f(p, g, g, None, g, g, g, None) == native.DCN_ERR_CUDA
