@@ -12,6 +12,7 @@ caller-allocated tensors, exactly like the C ABI.  :func:`core_fwd` and
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass, fields
@@ -20,6 +21,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdcn_b300.so")
+# the range-checked build (tests only)
+LIB_DEBUG_PATH = os.path.join(_HERE, "libdcn_b300_debug.so")
 
 DCN_F32, DCN_F16, DCN_BF16 = 0, 1, 2
 DCN_OK = 0
@@ -81,35 +84,52 @@ class Params:
 _lib = None
 
 
+def _open(path: str) -> ctypes.CDLL:
+    """Load a build of the library and declare its entry points' signatures."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with deformable_convolution_03_b300.build.build()")
+    L = ctypes.CDLL(path)
+    PP = ctypes.POINTER(dcn_params_t)
+    vp, ip = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
+    L.dcn_out_shape.argtypes = [PP, ip, ip]
+    L.dcn_num_points.argtypes = [PP]
+    L.dcn_core_fwd.argtypes = [PP, vp, vp, vp, vp, vp]
+    L.dcn_core_bwd_workspace.argtypes = [PP]
+    L.dcn_core_bwd_workspace.restype = ctypes.c_size_t
+    L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
+    L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
+    L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+    L.dcn_linear.argtypes = [ctypes.POINTER(dcn_linear_params_t), vp, vp, vp, vp, vp]
+    L.dcn_center_feature_scale.argtypes = [ctypes.POINTER(dcn_cfs_params_t), vp, vp, vp, vp, vp]
+    L.dcn_center_feature_scale_bwd.argtypes = [ctypes.POINTER(dcn_cfs_params_t)] + [vp] * 8
+    L.dcn_dwconv_ln_gelu.argtypes = [ctypes.POINTER(dcn_dwconv_params_t)] + [vp] * 7
+    L.dcn_status_str.argtypes = [ctypes.c_int]
+    L.dcn_status_str.restype = ctypes.c_char_p
+    return L
+
+
 def lib() -> ctypes.CDLL:
+    """The library every call in this module goes through (loaded on first use)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with deformable_convolution_03_b300.build.build()")
-        L = ctypes.CDLL(LIB_PATH)
-        PP = ctypes.POINTER(dcn_params_t)
-        vp, ip = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)
-        L.dcn_out_shape.argtypes = [PP, ip, ip]
-        L.dcn_num_points.argtypes = [PP]
-        L.dcn_core_fwd.argtypes = [PP, vp, vp, vp, vp, vp]
-        L.dcn_core_bwd_workspace.argtypes = [PP]
-        L.dcn_core_bwd_workspace.restype = ctypes.c_size_t
-        L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-        L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
-        L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
-        L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t,
-                                      vp]
-        L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
-        L.dcn_linear.argtypes = [ctypes.POINTER(dcn_linear_params_t), vp, vp, vp, vp, vp]
-        L.dcn_center_feature_scale.argtypes = [ctypes.POINTER(dcn_cfs_params_t), vp, vp, vp, vp,
-                                               vp]
-        L.dcn_center_feature_scale_bwd.argtypes = [ctypes.POINTER(dcn_cfs_params_t)] + [vp] * 8
-        L.dcn_dwconv_ln_gelu.argtypes = [ctypes.POINTER(dcn_dwconv_params_t)] + [vp] * 7
-        L.dcn_status_str.argtypes = [ctypes.c_int]
-        L.dcn_status_str.restype = ctypes.c_char_p
-        _lib = L
+        _lib = _open(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route this module's calls through another build of the library (the
+    range-checked one, in tests) for the duration of a with-block."""
+    global _lib
+    prev = _lib
+    _lib = _open(path)
+    try:
+        yield _lib
+    finally:
+        _lib = prev
 
 
 def _ptr(x) -> int | None:

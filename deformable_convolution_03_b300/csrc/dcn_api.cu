@@ -394,6 +394,37 @@ int cuda_status(cudaError_t e) {
   return DCN_ERR_CUDA;
 }
 
+// The status bits of the range checks seen by this thread's last call (the
+// DCN_DEBUG_BOUNDS build; a test hook reads them).
+thread_local unsigned g_last_bounds = 0;
+
+using BoundsReader = cudaError_t (*)(unsigned*);
+constexpr BoundsReader kBoundsReaders[] = {dcn::bounds_status_fwd, dcn::bounds_status_fwd_tma,
+                                           dcn::bounds_status_bwd, dcn::bounds_status_bwd_split,
+                                           dcn::bounds_status_dwconv};
+
+// The end of every call that launched work.  In the DCN_DEBUG_BOUNDS build:
+// wait for the stream, collect and clear the range checks' status words, and
+// report DCN_ERR_INTERNAL if any check failed; otherwise rc unchanged.
+int finish(int rc, void* stream) {
+#ifdef DCN_DEBUG_BOUNDS
+  if (rc != DCN_OK) return rc;
+  if (cuda_status(cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != DCN_OK)
+    return DCN_ERR_CUDA;
+  unsigned any = 0;
+  for (BoundsReader f : kBoundsReaders) {
+    unsigned v = 0;
+    if (cuda_status(f(&v)) != DCN_OK) return DCN_ERR_CUDA;
+    any |= v;
+  }
+  g_last_bounds = any;
+  return any ? DCN_ERR_INTERNAL : DCN_OK;
+#else
+  (void)stream;
+  return rc;
+#endif
+}
+
 }  // namespace
 
 extern "C" {
@@ -449,10 +480,12 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
   if (tile)
-    return cuda_status(dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset, mask,
-                                            output, static_cast<cudaStream_t>(stream)));
-  return cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
-                                     static_cast<cudaStream_t>(stream)));
+    return finish(cuda_status(dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset,
+                                                   mask, output, static_cast<cudaStream_t>(stream))),
+                  stream);
+  return finish(cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
+                                            static_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 }  // namespace
@@ -525,11 +558,13 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
     if (e != cudaSuccess) return DCN_ERR_CUDA;
   }
   if (scpt)
-    return cuda_status(dcn::launch_bwd_split(kp, wg, p->dtype, scpt, la, lb, grad_out, input,
-                                             offset, mask, acc, grad_input, grad_offset,
-                                             grad_mask, s));
-  return cuda_status(dcn::launch_bwd(kp, p->dtype, cpt, grad_out, input, offset, mask, acc,
-                                     grad_input, grad_offset, grad_mask, s));
+    return finish(cuda_status(dcn::launch_bwd_split(kp, wg, p->dtype, scpt, la, lb, grad_out,
+                                                    input, offset, mask, acc, grad_input,
+                                                    grad_offset, grad_mask, s)),
+                  s);
+  return finish(cuda_status(dcn::launch_bwd(kp, p->dtype, cpt, grad_out, input, offset, mask,
+                                            acc, grad_input, grad_offset, grad_mask, s)),
+                s);
 }
 
 }  // namespace
@@ -688,8 +723,9 @@ int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const
   const bool tc = dcn::options().linear_tc && dcn::linear_tc_ok(p->dtype, p->M, p->K, p->N,
                                                                    x, w, y);
   if (fault_injected()) return DCN_ERR_CUDA;
-  return cuda_status(dcn::launch_linear(p->dtype, p->M, p->K, p->N, x, w, bias, y, tc,
-                                        static_cast<cudaStream_t>(stream)));
+  return finish(cuda_status(dcn::launch_linear(p->dtype, p->M, p->K, p->N, x, w, bias, y, tc,
+                                        static_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 
@@ -703,8 +739,9 @@ int dcn_center_feature_scale(const dcn_cfs_params_t* p, const void* core, const 
     if (!aligned(q, es)) return DCN_ERR_ALIGN;
   const int vb = cfs_vbytes(p->C / p->G, es, false, {core, x_proj, out});
   if (fault_injected()) return DCN_ERR_CUDA;
-  return cuda_status(dcn::launch_cfs_fwd(p->dtype, vb, p->M, p->C, p->G, core, x_proj, logits,
-                                         out, static_cast<cudaStream_t>(stream)));
+  return finish(cuda_status(dcn::launch_cfs_fwd(p->dtype, vb, p->M, p->C, p->G, core, x_proj, logits,
+                                         out, static_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out,
@@ -722,9 +759,10 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
   const int vb = cfs_vbytes(p->C / p->G, es, true,
                             {grad_out, core, x_proj, grad_core, grad_x_proj});
   if (fault_injected()) return DCN_ERR_CUDA;
-  return cuda_status(dcn::launch_cfs_bwd(p->dtype, vb, p->M, p->C, p->G, grad_out, core, x_proj,
+  return finish(cuda_status(dcn::launch_cfs_bwd(p->dtype, vb, p->M, p->C, p->G, grad_out, core, x_proj,
                                          logits, grad_core, grad_x_proj, grad_logits,
-                                         static_cast<cudaStream_t>(stream)));
+                                         static_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* weight,
@@ -734,8 +772,9 @@ int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* 
   if (const int rc = dwconv_plan(p, x, weight, bias, gamma, beta, y, &d)) return rc;
   if ((long long)p->N * p->H * p->W == 0) return DCN_OK;
   if (fault_injected()) return DCN_ERR_CUDA;
-  return cuda_status(dcn::launch_dwconv(d, p->dtype, x, weight, bias, gamma, beta, y,
-                                        static_cast<cudaStream_t>(stream)));
+  return finish(cuda_status(dcn::launch_dwconv(d, p->dtype, x, weight, bias, gamma, beta, y,
+                                        static_cast<cudaStream_t>(stream))),
+                stream);
 }
 
 }  // extern "C"
@@ -799,3 +838,19 @@ extern "C" void dcn_internal_reset_options(void) { dcn::g_options = dcn::Options
 // Test hook: the cudaError_t behind the calling thread's last DCN_ERR_CUDA
 // from a CUDA call (0 if none).
 extern "C" int dcn_internal_last_cuda_error(void) { return g_last_cuda_error; }
+
+// Test hooks of the range checks: whether this is the DCN_DEBUG_BOUNDS build;
+// the status bits the calling thread's last call collected; and a status
+// word set from the host (the forward's), so that the next call's check of
+// the words can be seen to report DCN_ERR_INTERNAL and to clear them.
+extern "C" int dcn_internal_debug_bounds(void) {
+#ifdef DCN_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+extern "C" unsigned dcn_internal_bounds_status(void) { return g_last_bounds; }
+extern "C" int dcn_internal_set_bounds_status(unsigned v) {
+  return cuda_status(dcn::bounds_status_set_fwd(v));
+}

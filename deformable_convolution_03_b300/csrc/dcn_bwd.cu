@@ -117,6 +117,10 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
   }
   const T* mrow = mask + unit * kp.os_mask;
   const T* orow = offset + unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow)) {  // (checked build) read unit 0's rows
+    mrow = mask;
+    orow = offset;
+  }
   float mx = 0.f, inv = 1.f;
   if (kp.softmax && active) softmax_stats_b(mrow, kp.P, mx, inv);
 
@@ -162,7 +166,7 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
         const long long pix = img + (long long)(y0 + (k >> 1)) * kp.W + (x0 + (k & 1));
         const long long at = pix * kp.C + cbase;
         float v[CPT], g[CPT];
-        Slice<T, CPT>::load(input + at, v);
+        load_slice_in<T, CPT>(input + at, v, input, input_bytes<T>(kp));
         float s = 0.f;
 #pragma unroll
         for (int i = 0; i < CPT; ++i) {
@@ -170,7 +174,8 @@ bwd_kernel(const KParams kp, const T* __restrict__ gout, const T* __restrict__ i
           g[i] = w[k] * go[i];
         }
         dk[k] = s;
-        red_add<CPT>(gin + at, g);
+        if (DCN_IN_SPAN(gin + at, CPT * sizeof(float), gin, input_bytes<float>(kp), kBadScatter))
+          red_add<CPT>(gin + at, g);
       }
     }
     // sum the four corner dot products over the threads of the unit
@@ -229,6 +234,7 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
   const T* mrow = mask + unit * kp.os_mask;
   const T* orow = offset + unit * kp.os_off;
   const T* grow = gout + unit * kp.gc;
+  if (!rows_in(kp, offset, mask, orow, mrow) || !out_in(kp, gout, grow, kp.gc)) return;
   float mx = 0.f, inv = 1.f;
   if (kp.softmax) softmax_stats_b(mrow, kp.P, mx, inv);
   const float ref_x = (float)(u.wo * kp.stride_w - kp.pad_w + kp.cen_w);
@@ -255,6 +261,10 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
         if (!ok[k]) continue;
         const long long pix = img + (long long)(y0 + (k >> 1)) * kp.W + (x0 + (k & 1));
         const long long at = pix * kp.C + (long long)u.g * kp.gc;
+        if (!DCN_IN_SPAN(input + at, kp.gc * sizeof(T), input, input_bytes<T>(kp), kBadGather) ||
+            !DCN_IN_SPAN(gin + at, kp.gc * sizeof(float), gin, input_bytes<float>(kp),
+                         kBadScatter))
+          continue;
         for (int c = 0; c < kp.gc; ++c) {
           const float g = Dt<T>::one(grow + c);
           dk[k] = fmaf(g, Dt<T>::one(input + at + c), dk[k]);
@@ -295,6 +305,8 @@ bwd_generic_kernel(const KParams kp, const T* __restrict__ gout, const T* __rest
         if (!ok[k]) continue;
         const long long pix = img + (long long)(y0 + (k >> 1)) * kp.W + (x0 + (k & 1));
         const long long at = pix * kp.C + (long long)u.g * kp.gc;
+        if (!DCN_IN_SPAN(input + at, kp.gc * sizeof(T), input, input_bytes<T>(kp), kBadGather))
+          continue;
         float s = 0.f;
         for (int c = 0; c < kp.gc; ++c)
           s = fmaf(Dt<T>::one(grow + c), Dt<T>::one(input + at + c), s);
@@ -406,5 +418,7 @@ cudaError_t launch_bwd(const KParams& kp, int dtype, int cpt, const void* gout, 
     default: return cudaErrorInvalidValue;
   }
 }
+
+DCN_BOUNDS_READER(bwd)
 
 }  // namespace dcn

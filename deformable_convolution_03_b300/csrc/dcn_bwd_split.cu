@@ -99,6 +99,10 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
 
   const T* mrow = mask + (size_t)unit * kp.os_mask;
   const T* orow = offset + (size_t)unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow)) {  // (checked build) read unit 0's rows
+    mrow = mask;
+    orow = offset;
+  }
   const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
   const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
   const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
@@ -106,7 +110,7 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
   const float scale = kp.offset_scale;
 
   uint32_t gw[NW];
-  if (active) {
+  if (active && out_in(kp, gout, gout + (size_t)unit * kp.gc + c0, CPT)) {
     ldg_words<NW>(gout + (size_t)unit * kp.gc + c0, gw);
   } else {
 #pragma unroll
@@ -186,7 +190,7 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
     const bool ok[4] = {vy0 && vx0, vy0 && vx1, vy1 && vx0, vy1 && vx1};
     uint32_t v[4][NW];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ldg_words<NW>(img + off[k], v[k]);
+    for (int k = 0; k < 4; ++k) ldg_words_in<NW>(img + off[k], v[k], input, input_bytes<T>(kp));
     float dk[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -346,14 +350,19 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
   const size_t unit = active ? (((size_t)n * kp.Ho + ho) * kp.Wo + wo) * kp.G + g : 0;
   const T* mrow = mask + unit * kp.os_mask;
   const T* orow = offset + unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow)) {  // (checked build) read unit 0's rows
+    mrow = mask;
+    orow = offset;
+  }
   const size_t img_off = (size_t)n * kp.H * kp.W * kp.C + (size_t)g * kp.gc;
+  const size_t gin_bytes = input_bytes<float>(kp);
   const int W = kp.W, H = kp.H;
   const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
   const float ref_y = (float)(ho * kp.stride_h - kp.pad_h + kp.cen_h);
   const float scale = kp.offset_scale;
 
   uint32_t gw[NW];
-  if (active) {
+  if (active && out_in(kp, gout, gout + unit * kp.gc, CPT)) {
     ldg_words<NW>(gout + unit * kp.gc, gw);
   } else {
 #pragma unroll
@@ -426,6 +435,10 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
     const int cy = y0 - wy0, cx = x0 - wx0;
     if ((unsigned)cy < (unsigned)(wg.WH - 1) && (unsigned)cx < (unsigned)cw) {
       const int cell = cy * cw + cx;
+      if (!DCN_IN_SPAN(count + cell, sizeof(int), count, ncell * sizeof(int), kBadShared)) {
+        far |= 1u << p;
+        continue;
+      }
       code[p] = (atomicAdd(&count[cell], 1) << 16) | cell;
       if constexpr (k16) {
         wq[p].x = (uint32_t)Fma<T>::weight(w[0]) | ((uint32_t)Fma<T>::weight(w[1]) << 16);
@@ -469,6 +482,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
   for (int p = 0; p < P; ++p) {
     if (code[p] < 0) continue;
     const int o = head[code[p] & 0xffff] + (code[p] >> 16);
+    if (!DCN_IN_SPAN(eu + o, 2, eu, nsamp * 2, kBadShared)) continue;
     if constexpr (k16) {
       wa[o] = wq[p].y;
       wb[o] = wq[p].x;
@@ -523,8 +537,9 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
     // the weight of visit v for this pixel, and the visit's unit
     auto weight = [&](int v, int& un) -> typename Fma<T>::W {
       const bool in_a = v < na;
-      const int o = in_a ? sa + v : sb + (v - na);
+      int o = in_a ? sa + v : sb + (v - na);
       const bool right = o < (in_a ? ma : mb);
+      if (!DCN_IN_SPAN(eu + o, 2, eu, nsamp * 2, kBadShared)) o = 0;  // (checked build)
       const Wh h = (in_a ? wa : wb)[o];
       un = eu[o];
       // the right corner (x1) of the row: the high half, or .y
@@ -535,6 +550,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
       }
     };
     auto row = [&](int un, uint32_t (&vv)[NW]) {
+      if (!DCN_IN_SPAN(gos + un * NW, NW * 4, gos, nunit * NW * 4, kBadShared)) un = 0;
       const uint4* src = reinterpret_cast<const uint4*>(gos + un * NW);
 #pragma unroll
       for (int k = 0; k < NC; ++k) {
@@ -592,6 +608,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
       const int off = __shfl_sync(0xffffffffu, pix_off, g0 + r);
       if (!((got_any >> (g0 + r)) & 1u)) continue;
       float* dst = gin + img_off + (size_t)off * kp.C + 4 * j;
+      if (!DCN_IN_SPAN(dst, 16, gin, gin_bytes, kBadScatter)) continue;
       asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[4 * r]),
                    "f"(acc[4 * r + 1]), "f"(acc[4 * r + 2]), "f"(acc[4 * r + 3]));
     }
@@ -633,6 +650,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
         const int yy = y0 + (c >> 1), xx = x0 + (c & 1);
         if ((unsigned)yy >= (unsigned)H || (unsigned)xx >= (unsigned)W) continue;
         float* dst = gin + img_off + ((size_t)yy * W + xx) * kp.C;
+        if (!DCN_IN_SPAN(dst, CPT * sizeof(float), gin, gin_bytes, kBadScatter)) continue;
 #pragma unroll
         for (int i = 0; i < CPT; i += 4)
           asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i),
@@ -835,5 +853,7 @@ cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, in
     default: return cudaErrorInvalidValue;
   }
 }
+
+DCN_BOUNDS_READER(bwd_split)
 
 }  // namespace dcn

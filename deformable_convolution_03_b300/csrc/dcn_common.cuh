@@ -145,6 +145,58 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+// ---- range checks (the DCN_DEBUG_BOUNDS build) -------------------------------
+// Built with -DDCN_DEBUG_BOUNDS, every data-dependent access (a bilinear
+// corner gathered from the input or from a staged window, a grad_input
+// scatter, a row read or written at a computed index) first checks that its
+// bytes lie inside the tensor or buffer it belongs to.  An access that does
+// not is skipped (a load reads zeros) and sets a bit of this translation
+// unit's status word; the C ABI layer then synchronises after each call and
+// returns DCN_ERR_INTERNAL if any word is non-zero.  Nothing traps.  In the
+// normal build the checks compile to nothing and their arguments are dead.
+
+enum : unsigned {
+  kBadGather = 1u,   // a corner read from the input tensor
+  kBadShared = 2u,   // a read from a staged window or tile in shared memory
+  kBadScatter = 4u,  // a grad_input (accumulator) reduction
+  kBadStore = 8u,    // an output, grad_offset or grad_mask row
+  kBadRow = 16u,     // an offset, mask or upstream-gradient row
+  kBadStage = 32u,   // a staging copy's source or destination
+};
+
+#ifdef DCN_DEBUG_BOUNDS
+namespace {
+__device__ unsigned int g_bounds_status;
+}
+__device__ __forceinline__ bool in_span(const void* p, size_t n, const void* lo, size_t bytes,
+                                        unsigned bit) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(lo);
+  const bool ok = a >= b && a + n <= b + bytes;
+  if (!ok) atomicOr(&g_bounds_status, bit);
+  return ok;
+}
+#define DCN_IN_SPAN(p, n, lo, bytes, bit) ::dcn::in_span((p), (n), (lo), (bytes), (bit))
+// This translation unit's reader: copies the status word out and clears it.
+#define DCN_BOUNDS_READER(name)                                                          \
+  cudaError_t bounds_status_##name(unsigned* v) {                                        \
+    const unsigned zero = 0;                                                             \
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_bounds_status, sizeof(unsigned));          \
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bounds_status, &zero, sizeof zero);   \
+    return e;                                                                            \
+  }                                                                                      \
+  cudaError_t bounds_status_set_##name(unsigned v) {                                     \
+    return cudaMemcpyToSymbol(g_bounds_status, &v, sizeof v);                            \
+  }
+#else
+#define DCN_IN_SPAN(p, n, lo, bytes, bit) true
+#define DCN_BOUNDS_READER(name)                                                          \
+  cudaError_t bounds_status_##name(unsigned* v) {                                        \
+    *v = 0;                                                                              \
+    return cudaSuccess;                                                                  \
+  }                                                                                      \
+  cudaError_t bounds_status_set_##name(unsigned) { return cudaSuccess; }
+#endif
+
 // ---- storage dtype traits ---------------------------------------------------
 
 template <typename T> struct Dt;
@@ -288,6 +340,47 @@ struct Slice {
   }
 };
 
+// A slice gathered from the tensor [lo, lo + bytes) (checked in the
+// DCN_DEBUG_BOUNDS build; zeros if it lies outside).
+template <typename T, int CPT>
+__device__ __forceinline__ void load_slice_in(const T* p, float (&v)[CPT], const void* lo,
+                                              size_t bytes) {
+  if (!DCN_IN_SPAN(p, CPT * sizeof(T), lo, bytes, kBadGather)) {
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) v[i] = 0.f;
+    return;
+  }
+  Slice<T, CPT>::load(p, v);
+}
+
+// Bytes of the input tensor, and the spans of the offset and mask rows of
+// all units (row u starts at u * os elements; the last row ends its 2P or P
+// values in; a merged offset/mask tensor holds whole rows of os_off).
+template <typename T> __device__ __forceinline__ size_t input_bytes(const KParams& kp) {
+  return (size_t)kp.N * kp.H * kp.W * kp.C * sizeof(T);
+}
+template <typename T> __device__ __forceinline__ size_t offset_bytes(const KParams& kp) {
+  return (kp.merged ? (size_t)kp.units * kp.os_off
+                    : (size_t)(kp.units - 1) * kp.os_off + 2 * kp.P) * sizeof(T);
+}
+template <typename T> __device__ __forceinline__ size_t mask_bytes(const KParams& kp) {
+  return ((size_t)(kp.units - 1) * kp.os_mask + kp.P) * sizeof(T);
+}
+// The unit's offset and mask rows lie inside their tensors (always true in
+// the normal build).
+template <typename T>
+__device__ __forceinline__ bool rows_in(const KParams& kp, const T* offset, const T* mask,
+                                        const T* orow, const T* mrow) {
+  return DCN_IN_SPAN(orow, 2 * kp.P * sizeof(T), offset, offset_bytes<T>(kp), kBadRow) &&
+         DCN_IN_SPAN(mrow, kp.P * sizeof(T), mask, mask_bytes<T>(kp), kBadRow);
+}
+// The unit's row of gc values at out + unit * gc lies inside the output
+// (N*Ho*Wo*G rows).
+template <typename T>
+__device__ __forceinline__ bool out_in(const KParams& kp, const T* out, const T* row, int n) {
+  return DCN_IN_SPAN(row, n * sizeof(T), out, (size_t)kp.units * kp.gc * sizeof(T), kBadStore);
+}
+
 // ---- wide gathers: NW 32-bit words from a 32-byte-aligned address -----------
 
 template <int NW>
@@ -308,6 +401,19 @@ __device__ __forceinline__ void ldg_words(const void* p, uint32_t (&w)[NW]) {
       w[4 * i + 0] = u.x; w[4 * i + 1] = u.y; w[4 * i + 2] = u.z; w[4 * i + 3] = u.w;
     }
   }
+}
+
+// ldg_words of a corner inside the tensor [lo, lo + bytes) (checked in the
+// DCN_DEBUG_BOUNDS build; zeros if it is not).
+template <int NW>
+__device__ __forceinline__ void ldg_words_in(const void* p, uint32_t (&w)[NW], const void* lo,
+                                             size_t bytes) {
+  if (!DCN_IN_SPAN(p, 4 * NW, lo, bytes, kBadGather)) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) w[i] = 0u;
+    return;
+  }
+  ldg_words<NW>(p, w);
 }
 
 // N consecutive 32-bit words starting at the 4-byte aligned address p, read

@@ -197,6 +197,7 @@ dwconv_tile_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
   const int nfoot = fh * fw;
   const int fi0 = pix0 / fw, fj0 = pix0 - fi0 * fw;  // first pixel copied
   const int dfi = ppi / fw, dfj = ppi - dfi * fw;    // the step between pixels copied
+  const size_t x_bytes = (size_t)(total / tiles) * H * W * C * sizeof(T);  // (checked build)
   auto stage = [&](int t, int buf) {
     const int n = t / tiles;
     const int tile = t - n * tiles;
@@ -207,9 +208,13 @@ dwconv_tile_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
     const uint32_t dstep = (uint32_t)(ppi * C * sizeof(T));
     int i = i0 + fi0, j = j0 + fj0;
     for (int pix = pix0; pix < nfoot; pix += ppi, dst += dstep) {
-      const bool in = (unsigned)i < (unsigned)H && (unsigned)j < (unsigned)W;
-      cp_async16(dst, in ? (const void*)(xn + ((size_t)i * W + j) * C) : (const void*)x,
-                 in ? 16u : 0u);
+      bool in = (unsigned)i < (unsigned)H && (unsigned)j < (unsigned)W;
+      const T* src = xn + ((size_t)i * W + j) * C;
+      if (in && !DCN_IN_SPAN(src, 16, x, x_bytes, kBadStage)) in = false;
+      if (DCN_IN_SPAN(reinterpret_cast<const void*>((uintptr_t)dst), 16,
+                      reinterpret_cast<const void*>((uintptr_t)(smem_base + buf * foot_bytes)),
+                      foot_bytes, kBadStage))
+        cp_async16(dst, in ? (const void*)src : (const void*)x, in ? 16u : 0u);
       i += dfi;
       j += dfj;
       if (j >= j0 + fw) {
@@ -258,7 +263,11 @@ dwconv_tile_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
       const T* row = foot + fr * fw * C;
       float2 in[IW];
 #pragma unroll
-      for (int q = 0; q < IW; ++q) in[q] = two_f<T>(row + q * C);
+      for (int q = 0; q < IW; ++q)
+        in[q] = DCN_IN_SPAN(row + q * C, 2 * sizeof(T), smem + buf * foot_bytes, foot_bytes,
+                            kBadShared)
+                    ? two_f<T>(row + q * C)
+                    : make_float2(0.f, 0.f);
 #pragma unroll
       for (int py = 0; py < PY; ++py) {
         const int a = fr - py;
@@ -302,13 +311,17 @@ dwconv_tile_kernel(const T* __restrict__ x, const T* __restrict__ w, const T* __
 #pragma unroll
       for (int py = 0; py < PY; ++py, yp += row)
 #pragma unroll
-        for (int px = 0; px < kPX; ++px) put_two<T>(yp + px * C, acc[py][px]);
+        for (int px = 0; px < kPX; ++px)
+          if (DCN_IN_SPAN(yp + px * C, 2 * sizeof(T), y, x_bytes, kBadStore))
+            put_two<T>(yp + px * C, acc[py][px]);
     } else {
 #pragma unroll
       for (int py = 0; py < PY; ++py, yp += row)
 #pragma unroll
         for (int px = 0; px < kPX; ++px)
-          if (i0 + py < H && j0 + px < W) put_two<T>(yp + px * C, acc[py][px]);
+          if (i0 + py < H && j0 + px < W &&
+              DCN_IN_SPAN(yp + px * C, 2 * sizeof(T), y, x_bytes, kBadStore))
+            put_two<T>(yp + px * C, acc[py][px]);
     }
     __syncthreads();  // this buffer and red are rewritten in the next turn
   }
@@ -359,8 +372,9 @@ dwconv_general_kernel(const T* __restrict__ x, const T* __restrict__ w,
       for (int e = 0; e < k; ++e) {
         const int jj = j + e - r;
         if ((unsigned)jj >= (unsigned)W) continue;
-        acc = fmaf(ld_f<T>(w + (size_t)(a * k + e) * C + c), ld_f<T>(xn + ((size_t)ii * W + jj) * C + c),
-                   acc);
+        const T* src = xn + ((size_t)ii * W + jj) * C + c;
+        if (!DCN_IN_SPAN(src, sizeof(T), x, (size_t)pixels * C * sizeof(T), kBadGather)) continue;
+        acc = fmaf(ld_f<T>(w + (size_t)(a * k + e) * C + c), ld_f<T>(src), acc);
       }
     }
     buf[c] = acc;
@@ -378,6 +392,7 @@ dwconv_general_kernel(const T* __restrict__ x, const T* __restrict__ w,
   for (int o = 16; o >= 1; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   const float inv = 1.f / sqrtf(s2 / (float)C + eps);
   T* ym = y + (size_t)m * C;
+  if (!DCN_IN_SPAN(ym, C * sizeof(T), y, (size_t)pixels * C * sizeof(T), kBadStore)) return;
   for (int c = lane; c < C; c += 32) {
     const float z = fmaf((buf[c] - mean) * inv, ld_f<T>(gamma + c), ld_f<T>(beta + c));
     ym[c] = st_f<T>(gelu1(z));
@@ -453,6 +468,8 @@ cudaError_t launch_t(const DwGeom& d, const void* x, const void* w, const void* 
 }
 
 }  // namespace
+
+DCN_BOUNDS_READER(dwconv)
 
 size_t dwconv_smem_bytes(const DwGeom& d, int es) {
   if (!d.tiled) return (size_t)kGenWarps * d.C * sizeof(float);

@@ -66,6 +66,7 @@ fwd_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ 
 
   const T* mrow = mask + unit * kp.os_mask;
   const T* orow = offset + unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow)) return;
   float mx = 0.f, inv = 1.f;
   if (kp.softmax) softmax_stats(mrow, kp.P, mx, inv);
 
@@ -98,12 +99,13 @@ fwd_kernel(const KParams kp, const T* __restrict__ input, const T* __restrict__ 
       if (!ok[k]) continue;
       const long long pix = img + (long long)(y0 + (k >> 1)) * kp.W + (x0 + (k & 1));
       float v[CPT];
-      Slice<T, CPT>::load(input + pix * kp.C + cbase, v);
+      load_slice_in<T, CPT>(input + pix * kp.C + cbase, v, input, input_bytes<T>(kp));
 #pragma unroll
       for (int i = 0; i < CPT; ++i) acc[i] = fmaf(w[k], v[i], acc[i]);
     }
   }
-  Slice<T, CPT>::store(output + unit * kp.gc + c0, acc);
+  if (out_in(kp, output, output + unit * kp.gc + c0, CPT))
+    Slice<T, CPT>::store(output + unit * kp.gc + c0, acc);
 }
 
 // The wide kernel: one thread per (unit, slice of CPT channels) where a
@@ -153,6 +155,10 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
   const int P = KP > 0 ? KP : kp.P;
   const T* mrow = mask + (size_t)unit * kp.os_mask;
   const T* orow = offset + (size_t)unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow) ||
+      (KP == 9 && sizeof(T) == 2 && kp.merged_rows64 &&
+       !DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)))
+    return;
   const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
   const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
   const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
@@ -242,16 +248,17 @@ fwd_wide_kernel(const KParams kp, const T* __restrict__ input, const T* __restri
     const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
     const uint32_t ra = ya * WC, rb = yb * WC, ca = xa * C, cb = xb * C;
     uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
-    ldg_words<NW>(img + (ra + ca), v00);
-    ldg_words<NW>(img + (ra + cb), v01);
-    ldg_words<NW>(img + (rb + ca), v10);
-    ldg_words<NW>(img + (rb + cb), v11);
+    ldg_words_in<NW>(img + (ra + ca), v00, input, input_bytes<T>(kp));
+    ldg_words_in<NW>(img + (ra + cb), v01, input, input_bytes<T>(kp));
+    ldg_words_in<NW>(img + (rb + ca), v10, input, input_bytes<T>(kp));
+    ldg_words_in<NW>(img + (rb + cb), v11, input, input_bytes<T>(kp));
     fma_words<T, NW>(acc, v00, Fma<T>::weight(wy0 * wx0));
     fma_words<T, NW>(acc, v01, Fma<T>::weight(wy0 * wx1));
     fma_words<T, NW>(acc, v10, Fma<T>::weight(wy1 * wx0));
     fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1 * wx1));
   }
-  Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
+  if (out_in(kp, output, output + (size_t)unit * kp.gc + c0, CPT))
+    Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
 }
 
 template <typename T, int CPT>
@@ -305,5 +312,7 @@ cudaError_t launch_fwd(const KParams& kp, int dtype, int cpt, const void* in, co
     default: return cudaErrorInvalidValue;
   }
 }
+
+DCN_BOUNDS_READER(fwd)
 
 }  // namespace dcn

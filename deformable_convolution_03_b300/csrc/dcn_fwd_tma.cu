@@ -100,6 +100,10 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
   const int P = KP > 0 ? KP : kp.P;
   const T* mrow = mask + (size_t)unit * kp.os_mask;
   const T* orow = offset + (size_t)unit * kp.os_off;
+  if (!rows_in(kp, offset, mask, orow, mrow)) {  // (checked build) read unit 0's rows
+    mrow = mask;
+    orow = offset;
+  }
   const T* img = input + (size_t)n * kp.H * kp.W * kp.C + g * kp.gc + c0;
   const uint32_t W = kp.W, H = kp.H, C = kp.C, WC = (uint32_t)kp.W * kp.C;
   const float ref_x = (float)(wo * kp.stride_w - kp.pad_w + kp.cen_w);
@@ -191,7 +195,10 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
         for (int j = 0; j < NC; ++j) {
           // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
           // plain loads, so that the compiler may fold constant offsets
-          const uint4 c = *reinterpret_cast<const uint4*>(a00 + coff[j] + at[k]);
+          const unsigned char* q = a00 + coff[j] + at[k];
+          const uint4 c = DCN_IN_SPAN(q, 16, smem, tg.win_bytes, kBadShared)
+                              ? *reinterpret_cast<const uint4*>(q)
+                              : make_uint4(0u, 0u, 0u, 0u);
           v[4 * j] = c.x;
           v[4 * j + 1] = c.y;
           v[4 * j + 2] = c.z;
@@ -221,10 +228,10 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
       const uint32_t ya = min((uint32_t)y0, H - 1), yb = min((uint32_t)(y0 + 1), H - 1);
       const uint32_t ra = ya * WC, rbb = yb * WC, ca = xa * C, cb = xb * C;
       uint32_t v00[NW], v01[NW], v10[NW], v11[NW];
-      ldg_words<NW>(img + (ra + ca), v00);
-      ldg_words<NW>(img + (ra + cb), v01);
-      ldg_words<NW>(img + (rbb + ca), v10);
-      ldg_words<NW>(img + (rbb + cb), v11);
+      ldg_words_in<NW>(img + (ra + ca), v00, input, input_bytes<T>(kp));
+      ldg_words_in<NW>(img + (ra + cb), v01, input, input_bytes<T>(kp));
+      ldg_words_in<NW>(img + (rbb + ca), v10, input, input_bytes<T>(kp));
+      ldg_words_in<NW>(img + (rbb + cb), v11, input, input_bytes<T>(kp));
       rotate_chunks<NW>(v00, rot);
       rotate_chunks<NW>(v01, rot);
       rotate_chunks<NW>(v10, rot);
@@ -235,7 +242,8 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
       fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1v * wx1v));
     }
     unrotate_acc_t<CPT, T>(acc, rot);
-    Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
+    if (out_in(kp, output, output + (size_t)unit * kp.gc + c0, CPT))
+      Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
   }
   // a block whose wait ran out leaves no copy in flight into its memory
   if (!ready) mbar_wait_bounded(bar, 0, kWaitPolls);
@@ -343,5 +351,7 @@ cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& 
 cudaError_t read_wait_timeouts(unsigned long long* count) {
   return cudaMemcpyFromSymbol(count, g_wait_timeouts, sizeof(unsigned long long));
 }
+
+DCN_BOUNDS_READER(fwd_tma)
 
 }  // namespace dcn

@@ -85,4 +85,13 @@ size_t dwconv_smem_bytes(const DwGeom& d, int es);
 cudaError_t launch_dwconv(const DwGeom& d, int dtype, const void* x, const void* w, const void* b,
                           const void* g, const void* bt, void* y, cudaStream_t s);
 
+// The range checks' status word of each translation unit that has checks
+// (always 0 outside the DCN_DEBUG_BOUNDS build): read and clear; set.
+cudaError_t bounds_status_fwd(unsigned* v);
+cudaError_t bounds_status_fwd_tma(unsigned* v);
+cudaError_t bounds_status_bwd(unsigned* v);
+cudaError_t bounds_status_bwd_split(unsigned* v);
+cudaError_t bounds_status_dwconv(unsigned* v);
+cudaError_t bounds_status_set_fwd(unsigned v);
+
 }  // namespace dcn

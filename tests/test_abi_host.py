@@ -295,3 +295,18 @@ def test_dwconv_argument_errors(native, opts):
     # a valid call stops at the fault hook, before any CUDA call
     opts.set("fault_inject", 1)
     assert f(p, g, g, None, g, g, g, None) == native.DCN_ERR_CUDA
+
+
+# ---- the range-checked build ---------------------------------------------------
+
+def test_range_checked_build_exports_every_declared_symbol(native):
+    from deformable_convolution_03_b300 import build
+    path = build.build(debug_bounds=True)
+    with native.using_library(path) as L:
+        for n in declared_functions():
+            assert hasattr(L, n), n
+        L.dcn_internal_debug_bounds.restype = ctypes.c_int
+        assert L.dcn_internal_debug_bounds() == 1
+    L = native.lib()
+    L.dcn_internal_debug_bounds.restype = ctypes.c_int
+    assert L.dcn_internal_debug_bounds() == 0
