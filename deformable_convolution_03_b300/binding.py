@@ -35,8 +35,8 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
-           "dcn_linear", "dcn_center_feature_scale", "dcn_center_feature_scale_bwd",
-           "dcn_dwconv_ln_gelu", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
+           "dcn_core_fwd_proj", "dcn_linear", "dcn_center_feature_scale",
+           "dcn_center_feature_scale_bwd", "dcn_dwconv_ln_gelu", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
 DCN_NOALLOC_SCRATCH_BYTES = 32 << 20
 DCN_DW_MAX_KERNEL = 31
 DCN_DW_MAX_CHANNELS = 2048
@@ -101,6 +101,7 @@ def _open(path: str) -> ctypes.CDLL:
     L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
     L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
     L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
+    L.dcn_core_fwd_proj.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp]
     L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
     L.dcn_linear.argtypes = [ctypes.POINTER(dcn_linear_params_t), vp, vp, vp, vp, vp]
     L.dcn_center_feature_scale.argtypes = [ctypes.POINTER(dcn_cfs_params_t), vp, vp, vp, vp, vp]
@@ -335,6 +336,18 @@ def dcn_core_fwd_om(p: Params, input, offset_mask, row_stride: int, output, stre
     _check(lib().dcn_core_fwd_om(ctypes.byref(p.c()), _ptr(input), _ptr(offset_mask),
                                  int(row_stride), _ptr(output), _stream(stream)),
            "dcn_core_fwd_om")
+
+
+def dcn_core_fwd_proj(p: Params, input, feat, weight, bias, row_stride: int, output,
+                      offset_mask=None, stream=None) -> None:
+    """Raw entry point: the forward with the merged offset/mask projection
+    feat (N, Ho, Wo, K) x weight (G*row_stride, K)^T + bias in the same launch;
+    the rows are also written to offset_mask (N, Ho, Wo, G, row_stride) when
+    given."""
+    _check(lib().dcn_core_fwd_proj(ctypes.byref(p.c()), _ptr(input), _ptr(feat),
+                                   int(feat.shape[-1]), _ptr(weight), _ptr(bias),
+                                   int(row_stride), _ptr(output), _ptr(offset_mask),
+                                   _stream(stream)), "dcn_core_fwd_proj")
 
 
 def dcn_core_bwd_om(p: Params, grad_out, input, offset_mask, row_stride: int, grad_input,

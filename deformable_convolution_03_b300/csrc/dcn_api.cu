@@ -401,7 +401,7 @@ thread_local unsigned g_last_bounds = 0;
 using BoundsReader = cudaError_t (*)(unsigned*);
 constexpr BoundsReader kBoundsReaders[] = {dcn::bounds_status_fwd, dcn::bounds_status_fwd_tma,
                                            dcn::bounds_status_bwd, dcn::bounds_status_bwd_split,
-                                           dcn::bounds_status_dwconv};
+                                           dcn::bounds_status_dwconv, dcn::bounds_status_fwd_proj};
 
 // The end of every call that launched work.  In the DCN_DEBUG_BOUNDS build:
 // wait for the stream, collect and clear the range checks' status words, and
@@ -701,11 +701,12 @@ int dcn_version(void) { return 100; }
 
 int dcn_wait_timeouts(unsigned long long* count) {
   if (!count) return DCN_ERR_NULL;
-  unsigned long long a = 0, c = 0;
+  unsigned long long a = 0, c = 0, f = 0;
   if (dcn::read_wait_timeouts(&a) != cudaSuccess ||
-      dcn::read_linear_wait_timeouts(&c) != cudaSuccess)
+      dcn::read_linear_wait_timeouts(&c) != cudaSuccess ||
+      dcn::read_proj_wait_timeouts(&f) != cudaSuccess)
     return DCN_ERR_CUDA;
-  *count = a + c;
+  *count = a + c + f;
   return DCN_OK;
 }
 
@@ -765,6 +766,59 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
                 stream);
 }
 
+int dcn_core_fwd_proj(const dcn_params_t* p, const void* input, const void* feat, int K,
+                      const void* weight, const void* bias, int row_stride, void* output,
+                      void* offset_mask, void* stream) {
+  Geometry g;
+  int rc = validate(p, &g);
+  if (rc != DCN_OK) return rc;
+  if (row_stride < 3 * g.P || row_stride % 2 || K < 1) return DCN_ERR_SHAPE;
+  const long long nom = (long long)p->G * row_stride;
+  if (g.units == 0) return DCN_OK;
+  if (!input || !feat || !weight || !output) return DCN_ERR_NULL;
+  const size_t es = (size_t)elem_size(p->dtype);
+  for (const void* q : {input, feat, weight, (const void*)output})
+    if (!aligned(q, es)) return DCN_ERR_ALIGN;
+  if ((bias && !aligned(bias, es)) || (offset_mask && !aligned(offset_mask, 2 * es)))
+    return DCN_ERR_ALIGN;
+  const long long M = g.units / p->G;  // output pixels: the projection's rows
+  if (M > (1LL << 40) / K || M > (1LL << 40) / nom || nom > INT_MAX) return DCN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // the fused launch: 16-bit storage, a tile of the TMA forward, K a multiple
+  // of 64 up to 256, rows a multiple of 8 elements, 16-byte aligned tensors
+  const dcn::Options& o = dcn::options();
+  bool fused = o.fwd_proj && es == 2 && K % 64 == 0 && K <= 256 && row_stride % 8 == 0 &&
+               aligned(feat, 16) && aligned(weight, 16) && (!offset_mask || aligned(offset_mask, 16));
+  dcn::KParams kp;
+  fill_kparams(p, g, &kp);
+  kp.os_off = kp.os_mask = row_stride;
+  kp.merged = 1;
+  alignas(64) unsigned char map[128], fmap[128], wmap[128];
+  dcn::TileGeom tg;
+  dcn::ProjGeom pg;
+  int cpt = 0;
+  if (fused) {
+    cpt = pick_fwd_cpt(p, g, input, output);
+    fused = cpt < 0 &&
+            plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map,
+                          (size_t)std::max(1, o.fwd_proj_win) * 1024, o.fwd_any_tile != 0) &&
+            dcn::proj_plan(kp, tg, (int)es, K, row_stride, &pg) &&
+            dcn::encode_proj_maps(kp, pg, p->dtype, feat, K, weight, fmap, wmap);
+  }
+  if (fault_injected()) return DCN_ERR_CUDA;
+  if (fused)
+    return finish(cuda_status(dcn::launch_fwd_proj(map, fmap, wmap, kp, tg, pg, p->dtype, -cpt,
+                                                   input, bias, output, offset_mask, s)),
+                  stream);
+  // otherwise the two launches: the projection into offset_mask, then the core
+  if (!offset_mask) return DCN_ERR_UNSUPPORTED;
+  const dcn_linear_params_t lp{M, K, (int)nom, p->dtype};
+  rc = dcn_linear(&lp, feat, weight, bias, offset_mask, stream);
+  if (rc != DCN_OK) return rc;
+  return dcn_core_fwd_om(p, input, offset_mask, row_stride, output, stream);
+}
+
 int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* weight,
                        const void* bias, const void* gamma, const void* beta, void* y,
                        void* stream) {
@@ -802,6 +856,8 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_halo", &dcn::Options::fwd_halo},
     {"fwd_any_tile", &dcn::Options::fwd_any_tile},
     {"fwd_row64", &dcn::Options::fwd_row64},
+    {"fwd_proj", &dcn::Options::fwd_proj},
+    {"fwd_proj_win", &dcn::Options::fwd_proj_win},
     {"bwd_split", &dcn::Options::bwd_split},
     {"bwd_fuse", &dcn::Options::bwd_fuse},
     {"bwd_cpt", &dcn::Options::bwd_cpt},

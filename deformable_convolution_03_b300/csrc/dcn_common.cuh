@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/dcn_core.h"
 
 namespace dcn {
@@ -77,6 +79,16 @@ struct TileGeom {
   unsigned win_bytes;
 };
 
+// The forward with its offset/mask projection (dcn_fwd_proj.cu): K = 64 * KB
+// feature channels, row_stride rs, NB = GB * rs projection outputs per block
+// (tensor-memory columns ncols), the rows in shared memory om_stride elements
+// apart; byte offsets of the weight tiles, the window and the barriers in the
+// block's shared memory (after 1024-byte alignment), and its total.
+struct ProjGeom {
+  int KB, rs, NB, ncols, om_stride;
+  unsigned b_off, win_off, bar_off, om_bytes, smem_bytes;
+};
+
 // Shared memory of bwd_input_kernel: per sample (TH*TW*P), in cell order, its
 // four corner weights (4 x 16 bits for 16-bit storage, 4 x float32 otherwise)
 // and its 16-bit unit, the tile's grad_out (gc*es bytes per output
@@ -143,6 +155,61 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+// ---- tensor cores (tcgen05) ---------------------------------------------------
+
+// Shared-memory matrix descriptor of tcgen05.mma for a K-major operand in the
+// 128-byte swizzled layout: rows of 128 bytes (64 16-bit elements), groups of
+// 8 rows 1024 bytes apart.  Fields: start address >> 4 (bits 0-13), leading
+// byte offset (unused for this layout, 1), stride byte offset >> 4 (bits
+// 32-45), descriptor version 1 (bits 46-47), layout 2 = 128-byte swizzle
+// (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: float32 accumulator (bits
+// 4-5 = 1), A and B of format fmt (0 = f16, 1 = bf16; bits 7-9 and 10-12),
+// both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc(uint32_t fmt, uint32_t n, uint32_t m) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// 16 columns of one tensor-memory lane per thread, without waiting: the
+// caller issues several, then one tcgen05.wait::ld
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // ---- range checks (the DCN_DEBUG_BOUNDS build) -------------------------------

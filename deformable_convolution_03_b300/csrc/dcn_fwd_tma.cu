@@ -267,6 +267,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+void* tensor_map_encoder() { return reinterpret_cast<void*>(encoder()); }
+
 bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const void* input,
                       void* map_out) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();

@@ -50,6 +50,25 @@ cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& 
                             cudaStream_t s);
 // Blocks whose bounded wait for a tensor copy ran out, since load.
 cudaError_t read_wait_timeouts(unsigned long long* count);
+// The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000, to
+// be cast by the caller), or nullptr if the driver does not provide it.
+void* tensor_map_encoder();
+
+// The forward with the merged offset/mask projection in its prologue
+// (dcn_fwd_proj.cu), on a tile planned for the TMA forward: proj_plan fills
+// pg (false when the shape does not fit: 16-bit only, K a multiple of 64 up to
+// 256, NB a multiple of 16 up to 256, at most 128 tile pixels);
+// encode_proj_maps the tensor maps of the features (K, Wo, Ho, N) and of the
+// weight (K, G * row_stride); launch_fwd_proj runs it (bias may be null; om,
+// the merged rows written out, may be null).
+bool proj_plan(const KParams& kp, const TileGeom& tg, int es, int K, int rs, ProjGeom* pg);
+bool encode_proj_maps(const KParams& kp, const ProjGeom& pg, int dtype, const void* feat, int K,
+                      const void* w, void* fmap_out, void* wmap_out);
+cudaError_t launch_fwd_proj(const void* map, const void* fmap, const void* wmap,
+                            const KParams& kp, const TileGeom& tg, const ProjGeom& pg, int dtype,
+                            int cpt, const void* in, const void* bias, void* out, void* om,
+                            cudaStream_t s);
+cudaError_t read_proj_wait_timeouts(unsigned long long* count);
 
 // The linear projections (dcn_linear.cu): the tensor-core kernels when tc
 // (the shape and alignment checks of linear_tc_ok pass), else shared-memory
@@ -92,6 +111,7 @@ cudaError_t bounds_status_fwd_tma(unsigned* v);
 cudaError_t bounds_status_bwd(unsigned* v);
 cudaError_t bounds_status_bwd_split(unsigned* v);
 cudaError_t bounds_status_dwconv(unsigned* v);
+cudaError_t bounds_status_fwd_proj(unsigned* v);
 cudaError_t bounds_status_set_fwd(unsigned v);
 
 }  // namespace dcn

@@ -224,6 +224,39 @@ typedef struct {
 int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const void* bias,
                void* y, void* stream);
 
+/* DCNv4's forward with its merged offset/mask projection in the same launch.
+ * In the module the offsets and the mask are linear projections of the
+ * control features (page "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现
+ * 逐行解读", section 三 items 3-4), merged by DCNv4 into one layer whose rows
+ * are the offset_mask rows of dcn_core_fwd_om (page "告别DCNv3的卡顿：实测DCNv4在
+ * A100上3倍提速，手把手教你集成到FlashInternImage", section 1).  This call
+ * computes
+ *     offset_mask = feat weight^T + bias   (as dcn_linear: float32 sums, one
+ *                                           rounding to the storage type)
+ *     output      = dcn_core_fwd_om(input, offset_mask, row_stride)
+ * where each block of the forward computes its tile's rows on the tensor
+ * cores and keeps them in shared memory, so the rows never travel through
+ * memory unless asked for.
+ *   p            the core's geometry (Ho x Wo output pixels, G groups)
+ *   input        (N, H, W, G*gc) channels-last, read
+ *   feat         (N, Ho, Wo, K) the projection's input, read
+ *   weight       (G*row_stride, K) row-major, read; bias (G*row_stride) or NULL
+ *   row_stride   >= 3P and even, as dcn_core_fwd_om (rows: 2P offsets, P mask
+ *                values, padding)
+ *   output       (N, Ho, Wo, G*gc), fully overwritten
+ *   offset_mask  (N, Ho, Wo, G, row_stride) or NULL: when given, the rows are
+ *                also written there (the backward needs them)
+ * One dtype for all.  The single launch applies to float16 / bfloat16 with K
+ * a multiple of 64 up to 256, row_stride a multiple of 8, feat, weight and
+ * offset_mask 16-byte aligned and the input laid out for the tensor-copy
+ * forward; otherwise, with offset_mask given, the call runs dcn_linear into
+ * offset_mask and then dcn_core_fwd_om (same results), and without it
+ * returns DCN_ERR_UNSUPPORTED.
+ * Errors as dcn_core_fwd_om, plus DCN_ERR_SHAPE for K < 1. */
+int dcn_core_fwd_proj(const dcn_params_t* p, const void* input, const void* feat, int K,
+                      const void* weight, const void* bias, int row_stride, void* output,
+                      void* offset_mask, void* stream);
+
 /* The centre feature scale between the core op and output_proj (page
  * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
  * item 5; page "DCNv4高效实践指南：掌握可变形卷积的3倍速度提升技术", section
