@@ -336,13 +336,15 @@ int dcn_dwconv_ln_gelu(const dcn_dwconv_params_t* p, const void* x, const void* 
                        const void* bias, const void* gamma, const void* beta, void* y,
                        void* stream);
 
-/* Diagnostics of the asynchronous tensor copies some kernels use: the number
- * of thread blocks, since the library was loaded, whose bounded wait for such a
- * copy ran out on the current device.  Such a block computed its results from
- * global memory instead, so results stay correct; a non-zero count means a
- * copy took seconds, i.e. something is wrong with the device.  Reads a device
- * counter synchronously (the current device).  DCN_ERR_NULL for a NULL
- * count, DCN_ERR_CUDA if the read fails. */
+/* Diagnostics of the asynchronous tensor copies and tensor-core operations
+ * some kernels use: the number of thread blocks, since the library was
+ * loaded, whose bounded wait for such a copy or operation ran out on the
+ * current device.  A block of the tensor-copy forward then computed its
+ * results from global memory, so they stay correct; a block of a projection
+ * (dcn_linear, dcn_core_fwd_proj) computed nothing, so its outputs are not
+ * valid.  A non-zero count means a copy took seconds, i.e. something is wrong
+ * with the device.  Reads device counters synchronously (the current device).
+ * DCN_ERR_NULL for a NULL count, DCN_ERR_CUDA if the read fails. */
 int dcn_wait_timeouts(unsigned long long* count);
 
 /* A static, human-readable name for a dcn_status_t. */
