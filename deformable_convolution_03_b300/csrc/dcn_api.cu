@@ -800,11 +800,25 @@ int dcn_core_fwd_proj(const dcn_params_t* p, const void* input, const void* feat
   int cpt = 0;
   if (fused) {
     cpt = pick_fwd_cpt(p, g, input, output);
-    fused = cpt < 0 &&
-            plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map,
-                          (size_t)std::max(1, o.fwd_proj_win) * 1024, o.fwd_any_tile != 0) &&
-            dcn::proj_plan(kp, tg, (int)es, K, row_stride, &pg) &&
-            dcn::encode_proj_maps(kp, pg, p->dtype, feat, K, weight, fmap, wmap);
+    fused = cpt < 0;
+    bool planned = false;
+    if (fused && o.fwd_proj_ws) {
+      // the persistent kernel: the tile first (its shape does not depend on
+      // the budget), then the window that the other buffers leave room for
+      dcn::KParams k1 = kp;
+      dcn::TileGeom t1;
+      if (plan_fwd_tile(p, g, -cpt, input, &k1, &t1, map, 64 * 1024, o.fwd_any_tile != 0)) {
+        const size_t budget = dcn::proj_ws_window_budget(k1, t1, (int)es, K, row_stride);
+        planned = budget > 0 &&
+                  plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, budget, o.fwd_any_tile != 0) &&
+                  dcn::proj_plan_ws(kp, tg, (int)es, K, row_stride, -cpt, &pg);
+      }
+    }
+    if (fused && !planned)
+      planned = plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map,
+                              (size_t)std::max(1, o.fwd_proj_win) * 1024, o.fwd_any_tile != 0) &&
+                dcn::proj_plan(kp, tg, (int)es, K, row_stride, &pg);
+    fused = fused && planned && dcn::encode_proj_maps(kp, pg, p->dtype, feat, K, weight, fmap, wmap);
   }
   if (fault_injected()) return DCN_ERR_CUDA;
   if (fused)
@@ -858,6 +872,7 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_row64", &dcn::Options::fwd_row64},
     {"fwd_proj", &dcn::Options::fwd_proj},
     {"fwd_proj_win", &dcn::Options::fwd_proj_win},
+    {"fwd_proj_ws", &dcn::Options::fwd_proj_ws},
     {"bwd_split", &dcn::Options::bwd_split},
     {"bwd_fuse", &dcn::Options::bwd_fuse},
     {"bwd_cpt", &dcn::Options::bwd_cpt},

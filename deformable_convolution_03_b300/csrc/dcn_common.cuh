@@ -87,6 +87,11 @@ struct TileGeom {
 struct ProjGeom {
   int KB, rs, NB, ncols, om_stride;
   unsigned b_off, win_off, bar_off, om_bytes, smem_bytes;
+  // the persistent, warp-specialised kernel (ws != 0): S feature stages, two
+  // windows and two row buffers, their byte offsets and strides; the
+  // sampling warps of a block
+  int ws, S, sample_warps;
+  unsigned a_off, win_stride, rows_off, rows_stride;
 };
 
 // Shared memory of bwd_input_kernel: per sample (TH*TW*P), in cell order, its

@@ -62,6 +62,12 @@ void* tensor_map_encoder();
 // weight (K, G * row_stride); launch_fwd_proj runs it (bias may be null; om,
 // the merged rows written out, may be null).
 bool proj_plan(const KParams& kp, const TileGeom& tg, int es, int K, int rs, ProjGeom* pg);
+// The persistent, warp-specialised version: proj_ws_window_budget gives the
+// window budget its other buffers leave (0: none); proj_plan_ws fills pg
+// (pg->ws = 1) for a tile planned with that budget, false if it does not fit.
+size_t proj_ws_window_budget(const KParams& kp, const TileGeom& tg, int es, int K, int rs);
+bool proj_plan_ws(const KParams& kp, const TileGeom& tg, int es, int K, int rs, int cpt,
+                  ProjGeom* pg);
 bool encode_proj_maps(const KParams& kp, const ProjGeom& pg, int dtype, const void* feat, int K,
                       const void* w, void* fmap_out, void* wmap_out);
 cudaError_t launch_fwd_proj(const void* map, const void* fmap, const void* wmap,

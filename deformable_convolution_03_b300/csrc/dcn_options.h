@@ -19,7 +19,8 @@ struct Options {
   int fwd_any_tile = 1;   // tiles of any shape (else powers of two) for the TMA forward
   int fwd_row64 = 1;      // 256-bit loads of merged 64-byte offset/mask rows
   int fwd_proj = 1;       // the offset/mask projection inside the forward where it applies
-  int fwd_proj_win = 40;  // window budget (KB) of that fused forward (40 measured fastest)
+  int fwd_proj_win = 40;  // window budget (KB) of the per-tile fused forward (40 measured fastest)
+  int fwd_proj_ws = 1;    // the persistent, warp-specialised fused forward where it fits
   // backward
   int bwd_split = 2;      // 2: split kernels for 16-bit storage, 1: for any dtype, 0: never
   int bwd_fuse = 1;       // both split halves in one launch

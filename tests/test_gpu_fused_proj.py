@@ -89,16 +89,25 @@ STAGES = [("t_stage1_f16", 2, 64), ("t_stage2_bf16", 2, 128), ("t_stage3_bf16", 
           ("t_stage4_bf16", 4, 256), ("g_stage1_bf16", 1, 256), ("g_stage1_rc_bf16", 1, 128)]
 
 
+# the persistent, warp-specialised kernel (where its buffers fit) and the
+# per-tile kernel
+KERNELS = {"persistent": {}, "per_tile": {"fwd_proj_ws": 0}}
+
+
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("name,N,K", STAGES, ids=[s[0] for s in STAGES])
-def test_stage_shapes(name, N, K):
+def test_stage_shapes(name, N, K, kernel, opts):
+    opts.update(KERNELS[kernel])
     w = WORKLOADS[name].with_(N=N)
     _check(w, K, 24 if w.P == 8 else 32)
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
 @pytest.mark.parametrize("K", [64, 128, 192, 256])
 @pytest.mark.parametrize("sm,rc", [(0, 0), (1, 0), (1, 1)])
-def test_ragged_tiles(dt, K, sm, rc):
+def test_ragged_tiles(dt, K, sm, rc, kernel, opts):
+    opts.update(KERNELS[kernel])
     # 9 x 13 pixels: ragged tiles in both directions (rows of the projection's
     # tile past the image are computed and dropped)
     w = small(f"fp_{dt}_{K}_{sm}{rc}", dt, gc=16, G=4, N=2, H=9, W=13, softmax=sm,
@@ -106,8 +115,10 @@ def test_ragged_tiles(dt, K, sm, rc):
     _check(w, K, 24 if w.P == 8 else 32, seed=K + sm)
 
 
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
 @pytest.mark.parametrize("gc,G,rs", [(8, 8, 32), (32, 2, 40), (16, 8, 48)])
-def test_group_blocks_and_row_strides(gc, G, rs):
+def test_group_blocks_and_row_strides(gc, G, rs, kernel, opts):
+    opts.update(KERNELS[kernel])
     # several blocks per tile's groups (each projects its own groups' rows),
     # wider rows than 3P
     w = small(f"fp_g{gc}_{G}_{rs}", "bf16", gc=gc, G=G, N=2, H=12, W=10, offset_std=2.5)
@@ -121,6 +132,13 @@ def test_no_bias():
 
 def test_plane_smaller_than_tile():
     w = small("fp_small", "bf16", gc=16, G=4, N=3, H=3, W=5)
+    _check(w, 64, 32)
+
+
+def test_many_tiles_per_block():
+    # 64 images of 56 x 56: each persistent block walks about 21 tiles, so both
+    # buffers of every pipeline stage turn over many times
+    w = WORKLOADS["t_stage1_f16"]
     _check(w, 64, 32)
 
 
