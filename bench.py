@@ -369,10 +369,13 @@ def e2e_pipelined(case: Case, steps: int, flush: torch.Tensor) -> float:
 def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     """The layers around the core at the workload's shape: DCNv4's merged
     offset/mask projection (C -> G x row stride, P = 9 rows padded to 32) and
-    the output projection (C -> C) by dcn_linear, and the centre feature
-    scale's mix (dcn_center_feature_scale, forward and backward), on synthetic
-    inputs and weights, each timed alone with L2 flushed, against HBM on their
-    ideal bytes (each tensor read or written once)."""
+    the output projection (C -> C) by dcn_linear, the centre feature scale's
+    mix (dcn_center_feature_scale, forward and backward) and the offset
+    branch's feature step (dcn_dwconv_ln_gelu), on synthetic inputs and
+    weights, each timed alone with L2 flushed, against HBM on their ideal
+    bytes (each tensor read or written once); and the forward with its
+    projection in one launch (dcn_core_fwd_proj) beside the same work as two
+    launches."""
     dt = DTYPES[w.dtype]
     M, C = w.N * w.H_out * w.W_out, w.C
     rs = 32 if w.P == 9 else ((3 * w.P + 7) // 8) * 8
@@ -415,6 +418,25 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     out["dwconv_ln_gelu"] = {"shape": f"{w.N}x{w.H}x{w.W}x{C}, k{DW_KERNEL}", "ms": round(ms, 5),
                              "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
                              "ideal_bytes": ideal}
+    # the forward with DCNv4's merged offset/mask projection in its launch
+    # (features of C channels, rows of rs), beside the same work as two
+    # launches: the projection into the merged tensor, then the core on it
+    if es == 2 and C % 64 == 0 and C <= 256:
+        p = B.Params(dtype=B.TORCH_TO_DCN[dt], **w.params())
+        inp = make_inputs(w)["input"].to(dev)
+        feat = (torch.rand(w.N, w.H_out, w.W_out, C, generator=g) * 2 - 1).to(dt).to(dev)
+        wt = (torch.randn(w.G * rs, C, generator=g) / C ** 0.5).to(dt).to(dev)
+        bo = torch.randn(w.G * rs, generator=g).to(dt).to(dev)
+        y = torch.empty(w.N, w.H_out, w.W_out, C, dtype=dt, device=dev)
+        rows = torch.empty(w.N, w.H_out, w.W_out, w.G, rs, dtype=dt, device=dev)
+        fused = _time_alone(lambda: B.dcn_core_fwd_proj(p, inp, feat, wt, bo, rs, y, None), flush,
+                            reps)
+        two = _time_alone(lambda: (B.dcn_linear(feat.reshape(-1, C), wt, bo,
+                                                rows.reshape(-1, w.G * rs)),
+                                   B.dcn_core_fwd_om(p, inp, rows, rs, y)), flush, reps)
+        out["forward_with_projection"] = {
+            "shape": f"{M}x{C} -> {w.G}x{rs} rows, then the core", "ms": round(fused, 5),
+            "two_launches_ms": round(two, 5)}
     return out
 
 
@@ -561,7 +583,8 @@ def profile_proj(dev) -> int:
     scale forward and backward at stage 1 (200704 x 64, 4 gates, float16), and
     the offset branch's feature step (5 x 5 depthwise convolution, LayerNorm,
     GELU) at T stage 1 (64 x 56 x 56 x 64, float16) and G stage 1
-    (2 x 128 x 128 x 512, bfloat16)."""
+    (2 x 128 x 128 x 512, bfloat16), and the forward with its offset/mask
+    projection in one launch at T stage 1 (64 -> 4 x 32 rows, float16)."""
     g = torch.Generator().manual_seed(1)
     calls = []
     for M, K, N, dt in ((200704, 64, 128, torch.float16), (200704, 64, 64, torch.float16),
@@ -580,6 +603,15 @@ def profile_proj(dev) -> int:
              make_dwconv_inputs(N, H, H, C, DW_KERNEL, dt, seed=2).items()}
         calls.append(lambda t=t: B.dwconv_ln_gelu(t["x"], t["weight"], t["bias"], t["gamma"],
                                                   t["beta"]))
+    # the forward with its offset/mask projection in one launch, stage 1
+    w = WORKLOADS["t_stage1_f16"]
+    p = B.Params(dtype=B.DCN_F16, **w.params())
+    inp = make_inputs(w)["input"].to(dev)
+    feat = (torch.rand(w.N, w.H_out, w.W_out, 64, generator=g) * 2 - 1).half().to(dev)
+    wt = (torch.randn(w.G * 32, 64, generator=g) / 8).half().to(dev)
+    bo = torch.randn(w.G * 32, generator=g).half().to(dev)
+    y = torch.empty(w.N, w.H_out, w.W_out, w.C, dtype=torch.float16, device=dev)
+    calls.append(lambda: B.dcn_core_fwd_proj(p, inp, feat, wt, bo, 32, y, None))
     for f in calls:
         f()
         f()

@@ -89,6 +89,17 @@ def test_feature_step_checked(checked, dt, C, k):
     assert _status(checked) == 0
 
 
+@pytest.mark.parametrize("ws", [1, 0])
+@pytest.mark.parametrize("name,N,K", [("t_stage1_f16", 1, 64), ("g_stage1_bf16", 1, 256)])
+def test_forward_with_projection_checked(checked, name, N, K, ws, opts):
+    # the forward with its projection in one launch (persistent or per-tile)
+    import test_gpu_fused_proj as FP
+    opts.set("fwd_proj_ws", ws)
+    w = WORKLOADS[name].with_(N=N)
+    FP._check(w, K, 32)
+    assert _status(checked) == 0
+
+
 def test_status_word_reports_internal_error(checked):
     # a word set from the host: the next call collects it, reports
     # DCN_ERR_INTERNAL and clears it; the call after that is clean
