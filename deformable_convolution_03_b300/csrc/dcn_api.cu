@@ -546,6 +546,8 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
   if (row_stride) {
     kp.os_off = kp.os_mask = row_stride;
     kp.merged = 1;
+    kp.merged_rows64 = g.P == 9 && es == 2 && aligned(offset, 32) &&
+                       (row_stride * es) % 32 == 0 && dcn::options().fwd_row64;
   }
   dcn::WinGeom wg;
   int la = 0, lb = 0;
@@ -787,8 +789,13 @@ int dcn_core_fwd_proj(const dcn_params_t* p, const void* input, const void* feat
 
   // the fused launch: 16-bit storage, a tile of the TMA forward, K a multiple
   // of 64 up to 256, rows a multiple of 8 elements, 16-byte aligned tensors
+  // With offset_mask given, the projection and the core as two launches are
+  // faster at every measured shape (the rows then cost a trip through memory,
+  // but the forward reads them with wide loads at its full occupancy); the
+  // single launch serves calls without a rows buffer, which cannot allocate one.
   const dcn::Options& o = dcn::options();
-  bool fused = o.fwd_proj && es == 2 && K % 64 == 0 && K <= 256 && row_stride % 8 == 0 &&
+  bool fused = (o.fwd_proj == 2 || (o.fwd_proj == 1 && !offset_mask)) && es == 2 &&
+               K % 64 == 0 && K <= 256 && row_stride % 8 == 0 &&
                aligned(feat, 16) && aligned(weight, 16) && (!offset_mask || aligned(offset_mask, 16));
   dcn::KParams kp;
   fill_kparams(p, g, &kp);

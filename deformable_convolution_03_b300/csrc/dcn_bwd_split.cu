@@ -125,8 +125,18 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
   bool vec = false;
   // (not for 64-byte float32 slices, whose corners already fill the registers)
   constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
-  if constexpr (kVecRows)
-    vec = active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
+  if constexpr (kVecRows) {
+    if (!kp.merged) {
+      vec = active && rows.load(offset, mask, kp.units, orow, mrow);
+    } else if constexpr (KP == 9 && sizeof(T) == 2) {
+      // DCNv4's merged 64-byte rows: the whole row in two 256-bit loads
+      if (active && kp.merged_rows64 &&
+          DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)) {
+        rows.load_merged64(orow);
+        vec = true;
+      }
+    }
+  }
 
   float mx = 0.f, inv = 1.f;
   if (kp.softmax && active) {
@@ -401,7 +411,17 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
     bool done = false;
     if constexpr (KP > 0) {
       UnitRows<T, KP> rows;
-      if (active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow)) {
+      bool got = false;
+      if (active && !kp.merged) {
+        got = rows.load(offset, mask, kp.units, orow, mrow);
+      } else if constexpr (KP == 9 && sizeof(T) == 2) {
+        if (active && kp.merged_rows64 &&
+            DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)) {
+          rows.load_merged64(orow);
+          got = true;
+        }
+      }
+      if (got) {
 #pragma unroll
         for (int p = 0; p < KP; ++p) {
           dd[p] = rows.off(p);

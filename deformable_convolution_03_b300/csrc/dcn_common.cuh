@@ -553,6 +553,19 @@ struct UnitRows {
     }
     return true;
   }
+  // A merged 64-byte row (P = 9, 16-bit storage, row stride 32 elements,
+  // 32-byte aligned): 2P offsets then P mask values read with two 256-bit
+  // loads.  Offset pair p is word p; mask value p is half 18 + p, i.e. the
+  // same words and halves as the separate mask row after its shift.
+  __device__ __forceinline__ void load_merged64(const T* orow) {
+    static_assert(KP == 9 && kEs == 2, "64-byte merged rows hold P = 9 16-bit rows");
+    uint32_t w[16];
+    ldg_words<16>(orow, w);
+#pragma unroll
+    for (int i = 0; i < NO; ++i) ow[i] = w[i];
+#pragma unroll
+    for (int i = 0; i < NM; ++i) mw[i] = w[NO + i];
+  }
   __device__ __forceinline__ float2 off(int p) const {
     if constexpr (kEs == 2) {
       float f[2];

@@ -113,8 +113,18 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
   UnitRows<T, KP> rows;
   bool vec = false;
   constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
-  if constexpr (kVecRows)
-    vec = active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
+  if constexpr (kVecRows) {
+    if (!kp.merged) {
+      vec = active && rows.load(offset, mask, kp.units, orow, mrow);
+    } else if constexpr (KP == 9 && sizeof(T) == 2) {
+      // DCNv4's merged 64-byte rows: the whole row in two 256-bit loads
+      if (active && kp.merged_rows64 &&
+          DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)) {
+        rows.load_merged64(orow);
+        vec = true;
+      }
+    }
+  }
 
   float mx = 0.f, inv = 1.f;
   if (kp.softmax && active) {

@@ -246,12 +246,14 @@ int dcn_linear(const dcn_linear_params_t* p, const void* x, const void* w, const
  *   output       (N, Ho, Wo, G*gc), fully overwritten
  *   offset_mask  (N, Ho, Wo, G, row_stride) or NULL: when given, the rows are
  *                also written there (the backward needs them)
- * One dtype for all.  The single launch applies to float16 / bfloat16 with K
- * a multiple of 64 up to 256, row_stride a multiple of 8, feat, weight and
- * offset_mask 16-byte aligned and the input laid out for the tensor-copy
- * forward; otherwise, with offset_mask given, the call runs dcn_linear into
- * offset_mask and then dcn_core_fwd_om (same results), and without it
- * returns DCN_ERR_UNSUPPORTED.
+ * One dtype for all.  With offset_mask given, the call runs dcn_linear into
+ * offset_mask and then dcn_core_fwd_om: two launches, measured faster than
+ * the single one at every shape tried.  Without it, the single launch runs;
+ * it applies to float16 / bfloat16 with K a multiple of 64 up to 256,
+ * row_stride a multiple of 8, feat and weight 16-byte aligned and the input
+ * laid out for the tensor-copy forward, and other calls without offset_mask
+ * return DCN_ERR_UNSUPPORTED.  Both ways compute the same rows (bit for bit)
+ * and the same forward on them.
  * Errors as dcn_core_fwd_om, plus DCN_ERR_SHAPE for K < 1. */
 int dcn_core_fwd_proj(const dcn_params_t* p, const void* input, const void* feat, int K,
                       const void* weight, const void* bias, int row_stride, void* output,

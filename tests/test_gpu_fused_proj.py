@@ -53,7 +53,7 @@ def _run(w, inp, feat, wt, b, rs, with_rows=True):
     return out.t, rows.t if rows is not None else None
 
 
-def _check(w, K, rs, bias=True, seed=3):
+def _check(w, K, rs, bias=True, seed=3, same_kernel=True):
     inp = make_inputs(w)["input"]
     feat, wt, b = _layer(w, K, rs, seed)
     if not bias:
@@ -76,9 +76,14 @@ def _check(w, K, rs, bias=True, seed=3):
     expect = oracle.forward(oracle_params(w), f64(inp), np.ascontiguousarray(off),
                             np.ascontiguousarray(msk))
     assert_close(out, expect, w.dtype, f"{w.name} fused output")
-    # the same launch without writing the rows gives the same output
+    # the same launch without writing the rows gives the same output; when
+    # the call takes another kernel without them, that output meets the oracle
+    # on the same rows
     out2, _ = _run(w, inp, feat, wt, b, rs, with_rows=False)
-    assert torch.equal(out, out2)
+    if same_kernel:
+        assert torch.equal(out, out2)
+    else:
+        assert_close(out2, expect, w.dtype, f"{w.name} single-launch output")
     return out
 
 
@@ -91,7 +96,9 @@ STAGES = [("t_stage1_f16", 2, 64), ("t_stage2_bf16", 2, 128), ("t_stage3_bf16", 
 
 # the persistent, warp-specialised kernel (where its buffers fit) and the
 # per-tile kernel
-KERNELS = {"persistent": {}, "per_tile": {"fwd_proj_ws": 0}}
+# (the fwd_proj switch at 2 keeps the single launch although offset_mask is
+# given, so that its rows can be checked)
+KERNELS = {"persistent": {"fwd_proj": 2}, "per_tile": {"fwd_proj": 2, "fwd_proj_ws": 0}}
 
 
 @pytest.mark.parametrize("kernel", sorted(KERNELS))
@@ -125,27 +132,39 @@ def test_group_blocks_and_row_strides(gc, G, rs, kernel, opts):
     _check(w, 64, rs)
 
 
-def test_no_bias():
+def test_no_bias(opts):
+    opts.set("fwd_proj", 2)
     w = small("fp_nobias", "f16", gc=16, G=4, N=1, H=16, W=16)
     _check(w, 128, 32, bias=False)
 
 
-def test_plane_smaller_than_tile():
+def test_plane_smaller_than_tile(opts):
+    opts.set("fwd_proj", 2)
     w = small("fp_small", "bf16", gc=16, G=4, N=3, H=3, W=5)
     _check(w, 64, 32)
 
 
-def test_many_tiles_per_block():
+def test_many_tiles_per_block(opts):
     # 64 images of 56 x 56: each persistent block walks about 21 tiles, so both
     # buffers of every pipeline stage turn over many times
+    opts.set("fwd_proj", 2)
     w = WORKLOADS["t_stage1_f16"]
     _check(w, 64, 32)
+
+
+@pytest.mark.parametrize("name,N,K", [("t_stage1_f16", 2, 64), ("g_stage1_bf16", 1, 256)])
+def test_default_policy(name, N, K):
+    # by default a call with offset_mask runs the two launches and one without
+    # runs the single launch: the same rows, the same output
+    w = WORKLOADS[name].with_(N=N)
+    _check(w, K, 32, same_kernel=False)
 
 
 @pytest.mark.parametrize("why", ["switch", "k96", "f32"])
 def test_two_launch_fallback(why, opts):
     # outside the single launch (switched off, K not a multiple of 64, float32)
-    # the call projects into offset_mask and runs the core on it: same checks
+    # the call projects into offset_mask and runs the core on it: same checks;
+    # without offset_mask such a call is refused
     dt = "f32" if why == "f32" else "bf16"
     K = 96 if why == "k96" else 64
     if why == "switch":

@@ -94,7 +94,7 @@ def test_feature_step_checked(checked, dt, C, k):
 def test_forward_with_projection_checked(checked, name, N, K, ws, opts):
     # the forward with its projection in one launch (persistent or per-tile)
     import test_gpu_fused_proj as FP
-    opts.set("fwd_proj_ws", ws)
+    opts.update({"fwd_proj": 2, "fwd_proj_ws": ws})
     w = WORKLOADS[name].with_(N=N)
     FP._check(w, K, 32)
     assert _status(checked) == 0
