@@ -367,6 +367,13 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     }
   }
   if (best < 0 || (long long)p->N * p->G * wg->tiles_h * wg->tiles_w > INT_MAX) return 0;
+  // one input block per (image, group) plane, its window covering every
+  // bilinear cell that touches the image (cells y0 in [-1, H-1], x0 in
+  // [-1, W-1]): that block alone sums the plane's grad_input and writes it in
+  // the storage type, with no float32 accumulator to clear and round
+  wg->direct = dcn::options().bwd_direct && wg->tiles_h == 1 && wg->tiles_w == 1 &&
+               wg->org_y <= -1 && wg->org_x <= -1 && wg->org_y + wg->WH - 2 >= p->H - 1 &&
+               wg->org_x + wg->WW - 2 >= p->W - 1;
   // the sample blocks read their corners through L1 over the wide forward's
   // tiles (staging their windows by a tensor copy measured slower inside the
   // fused launch: FlashInternImage-T stage 1 315-326 us against 272 us, the
@@ -549,13 +556,13 @@ int core_bwd(const dcn_params_t* p, const void* grad_out, const void* input, con
     kp.merged_rows64 = g.P == 9 && es == 2 && aligned(offset, 32) &&
                        (row_stride * es) % 32 == 0 && dcn::options().fwd_row64;
   }
-  dcn::WinGeom wg;
+  dcn::WinGeom wg{};
   int la = 0, lb = 0;
   const int scpt = plan_split(p, g, input, grad_out, acc, &kp, &wg, &la, &lb);
   const int cpt = scpt ? 0 : pick_bwd_cpt(p, input, grad_out, acc);
   if (fault_injected()) return DCN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (g.n_in > 0) {
+  if (g.n_in > 0 && !(scpt && wg.direct)) {
     cudaError_t e = cudaMemsetAsync(acc, 0, acc_bytes, s);
     if (e != cudaSuccess) return DCN_ERR_CUDA;
   }
@@ -885,6 +892,7 @@ constexpr OptionName kOptionNames[] = {
     {"bwd_cpt", &dcn::Options::bwd_cpt},
     {"bwd_halo", &dcn::Options::bwd_halo},
     {"bwd_stage", &dcn::Options::bwd_stage},
+    {"bwd_direct", &dcn::Options::bwd_direct},
     {"linear_tc", &dcn::Options::linear_tc},
     {"linear_bn", &dcn::Options::linear_bn},
     {"linear_yb", &dcn::Options::linear_yb},

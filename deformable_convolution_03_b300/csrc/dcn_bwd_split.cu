@@ -313,7 +313,7 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
                                             const T* __restrict__ gout,
                                             const T* __restrict__ offset,
                                             const T* __restrict__ mask, float* __restrict__ gin,
-                                            const unsigned bid) {
+                                            T* __restrict__ gdirect, const unsigned bid) {
   constexpr int CPT = NW * 4 / (int)sizeof(T);  // = gc
   constexpr int KPN = KP > 0 ? KP : 16;
   constexpr bool k16 = sizeof(T) == 2;
@@ -620,17 +620,32 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
         }
       }
     }
-    const unsigned got_any = __ballot_sync(0xffffffffu, nv > 0);
     const int pix_off = valid ? yy * W + xx : 0;
     const int g0 = lane & ~(L - 1);
+    if (wg.direct) {
+      // this block alone sums the plane's pixels: every pixel of the image
+      // written once, in the storage type, zeros included
+      const unsigned live = __ballot_sync(0xffffffffu, valid);
 #pragma unroll
-    for (int r = 0; r < L; ++r) {
-      const int off = __shfl_sync(0xffffffffu, pix_off, g0 + r);
-      if (!((got_any >> (g0 + r)) & 1u)) continue;
-      float* dst = gin + img_off + (size_t)off * kp.C + 4 * j;
-      if (!DCN_IN_SPAN(dst, 16, gin, gin_bytes, kBadScatter)) continue;
-      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[4 * r]),
-                   "f"(acc[4 * r + 1]), "f"(acc[4 * r + 2]), "f"(acc[4 * r + 3]));
+      for (int r = 0; r < L; ++r) {
+        const int off = __shfl_sync(0xffffffffu, pix_off, g0 + r);
+        if (!((live >> (g0 + r)) & 1u)) continue;
+        T* dst = gdirect + img_off + (size_t)off * kp.C + 4 * j;
+        if (!DCN_IN_SPAN(dst, 4 * sizeof(T), gdirect, input_bytes<T>(kp), kBadStore)) continue;
+        float q[4] = {acc[4 * r], acc[4 * r + 1], acc[4 * r + 2], acc[4 * r + 3]};
+        Slice<T, 4>::store(dst, q);
+      }
+    } else {
+      const unsigned got_any = __ballot_sync(0xffffffffu, nv > 0);
+#pragma unroll
+      for (int r = 0; r < L; ++r) {
+        const int off = __shfl_sync(0xffffffffu, pix_off, g0 + r);
+        if (!((got_any >> (g0 + r)) & 1u)) continue;
+        float* dst = gin + img_off + (size_t)off * kp.C + 4 * j;
+        if (!DCN_IN_SPAN(dst, 16, gin, gin_bytes, kBadScatter)) continue;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(acc[4 * r]),
+                     "f"(acc[4 * r + 1]), "f"(acc[4 * r + 2]), "f"(acc[4 * r + 3]));
+      }
     }
   }
   // far samples (rare): the point again, its four corners straight to memory.
@@ -685,8 +700,8 @@ template <typename T, int NW, int KP>
 __global__ void __launch_bounds__(256, NW <= 8 ? 3 : 2)
 bwd_input_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
                  const T* __restrict__ offset, const T* __restrict__ mask,
-                 float* __restrict__ gin) {
-  input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, blockIdx.x);
+                 float* __restrict__ gin, T* __restrict__ gdirect) {
+  input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, gdirect, blockIdx.x);
 }
 
 // Both halves in one launch: their blocks interleaved one to one (then the
@@ -699,7 +714,8 @@ __global__ void __launch_bounds__(256, 3)
 bwd_both_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
                 const T* __restrict__ input, const T* __restrict__ offset,
                 const T* __restrict__ mask, T* __restrict__ goff, T* __restrict__ gmask, int la,
-                int lb, float* __restrict__ gin, unsigned n_sample, unsigned n_input) {
+                int lb, float* __restrict__ gin, T* __restrict__ gdirect, unsigned n_sample,
+                unsigned n_input) {
   const unsigned b = blockIdx.x, m = min(n_sample, n_input);
   bool sample;
   unsigned id;
@@ -713,7 +729,7 @@ bwd_both_kernel(const KParams kp, const WinGeom wg, const T* __restrict__ gout,
   if (sample)
     sample_block<T, CPT, KP>(kp, gout, input, offset, mask, goff, gmask, la, lb, id);
   else
-    input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, id);
+    input_block<T, NW, KP>(kp, wg, gout, offset, mask, gin, gdirect, id);
 }
 
 
@@ -749,7 +765,7 @@ static cudaError_t launch_sample_t(const KParams& kp, const T* go_, const T* i_,
 
 template <typename T, int NW>
 static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T* go_,
-                                  const T* o_, const T* m_, float* acc, cudaStream_t s) {
+                                  const T* o_, const T* m_, float* acc, T* gin_, cudaStream_t s) {
   const size_t smem = split_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
   auto k9 = bwd_input_kernel<T, NW, 9>;
   auto k8 = bwd_input_kernel<T, NW, 8>;
@@ -765,7 +781,7 @@ static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T*
   }
   const long long blocks = (long long)kp.N * kp.G * wg.tiles_h * wg.tiles_w;
   if (blocks > INT_MAX) return cudaErrorInvalidConfiguration;
-  k<<<(unsigned)blocks, 256, smem, s>>>(kp, wg, go_, o_, m_, acc);
+  k<<<(unsigned)blocks, 256, smem, s>>>(kp, wg, go_, o_, m_, acc, gin_);
   return cudaGetLastError();
 }
 
@@ -773,7 +789,7 @@ static cudaError_t launch_input_t(const KParams& kp, const WinGeom& wg, const T*
 template <typename T, int CPT, int NW>
 static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* go_, const T* i_,
                                  const T* o_, const T* m_, T* goff_, T* gm_, int la, int lb,
-                                 float* acc, cudaStream_t s) {
+                                 float* acc, T* gin_, cudaStream_t s) {
   const int chunks = kp.gc / CPT;
   const int block = 256;
   const long long na = kp.tile_w > 0 ? (long long)kp.N * kp.tiles_w * kp.tiles_h
@@ -791,7 +807,7 @@ static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* 
     if (e != cudaSuccess) return e;
   }
   k<<<(unsigned)(na + nb), block, smem, s>>>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc,
-                                             (unsigned)na, (unsigned)nb);
+                                             gin_, (unsigned)na, (unsigned)nb);
   return cudaGetLastError();
 }
 
@@ -805,31 +821,32 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
   const T* m_ = static_cast<const T*>(msk);
   T* goff_ = static_cast<T*>(goff);
   T* gm_ = static_cast<T*>(gmask);
+  T* gin_ = static_cast<T*>(gin);
   cudaError_t e;
   const int nw = kp.gc * (int)sizeof(T) / 4;
   if (options().bwd_fuse) {
     // the (channels per sample thread, words per unit row) pairs that occur
     if constexpr (sizeof(T) == 2) {
       if (cpt == 8 && nw == 4)
-        e = launch_both_t<T, 8, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 8, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else if (cpt == 16 && nw == 8)
-        e = launch_both_t<T, 16, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 16, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else if (cpt == 16 && nw == 16)
-        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else
         return cudaErrorInvalidValue;
     } else {
       if (cpt == 4 && nw == 4)
-        e = launch_both_t<T, 4, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 4, 4>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else if (cpt == 8 && nw == 8)
-        e = launch_both_t<T, 8, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 8, 8>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else if (cpt == 16 && nw == 16)
-        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, s);
+        e = launch_both_t<T, 16, 16>(kp, wg, go_, i_, o_, m_, goff_, gm_, la, lb, acc, gin_, s);
       else
         return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    if ((void*)acc != gin) {
+    if ((void*)acc != gin && !wg.direct) {
       const int dt = std::is_same<T, __half>::value ? DCN_F16 : DCN_BF16;
       return launch_round(dt, acc, gin, (long long)kp.N * kp.H * kp.W * kp.C, s);
     }
@@ -843,13 +860,13 @@ static cudaError_t launch_split(const KParams& kp, const WinGeom& wg, int cpt, i
   }
   if (e != cudaSuccess) return e;
   switch (nw) {
-    case 4: e = launch_input_t<T, 4>(kp, wg, go_, o_, m_, acc, s); break;
-    case 8: e = launch_input_t<T, 8>(kp, wg, go_, o_, m_, acc, s); break;
-    case 16: e = launch_input_t<T, 16>(kp, wg, go_, o_, m_, acc, s); break;
+    case 4: e = launch_input_t<T, 4>(kp, wg, go_, o_, m_, acc, gin_, s); break;
+    case 8: e = launch_input_t<T, 8>(kp, wg, go_, o_, m_, acc, gin_, s); break;
+    case 16: e = launch_input_t<T, 16>(kp, wg, go_, o_, m_, acc, gin_, s); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  if ((void*)acc != gin) {
+  if ((void*)acc != gin && !wg.direct) {
     const int dt = std::is_same<T, __half>::value ? DCN_F16 : DCN_BF16;
     return launch_round(dt, acc, gin, (long long)kp.N * kp.H * kp.W * kp.C, s);
   }

@@ -65,6 +65,11 @@ struct WinGeom {
   int tiles_h, tiles_w;
   int WH, WW;
   int org_y, org_x;
+  // 1 when one tile covers each (image, group) plane and its window covers
+  // every bilinear cell that touches the image: the plane's grad_input then
+  // comes from one block alone, which writes it in the storage type directly
+  // (no float32 accumulator to clear, reduce into and round)
+  int direct;
 };
 
 // Geometry of the TMA-staged forward (fwd_tile_kernel): a block covers the

@@ -27,6 +27,7 @@ struct Options {
   int bwd_cpt = 4;        // largest slice of the single-pass kernel
   int bwd_halo = 6;       // halo (pixels) of the split input blocks' windows
   int bwd_stage = 1;      // gradient rows staged in shared memory
+  int bwd_direct = 1;     // planes one input block covers: grad_input written directly
   // projections
   int linear_tc = 1;       // tensor-core kernels where they apply
   int linear_bn = 256;     // largest output tile width of the K-loop kernel

@@ -196,6 +196,9 @@ BWD_MODES = {
     "split_unfused": {"bwd_split": 1, "bwd_fuse": 0},
     # the single-pass atomic kernels
     "single_pass": {"bwd_split": 0},
+    # the split kernels reducing into the float32 accumulator even where one
+    # input block covers a whole plane (and would write grad_input directly)
+    "split_accumulate": {"bwd_split": 1, "bwd_direct": 0},
 }
 
 
