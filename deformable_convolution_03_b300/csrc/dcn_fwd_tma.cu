@@ -59,8 +59,10 @@ __device__ __forceinline__ void unrotate_acc_t(float (&acc)[CPT], int rot) {
 }
 
 // RB: the bytes of one window pixel (GB * gc * sizeof(T)) when known at compile
-// time (128, the usual case), else 0.
-template <typename T, int CPT, int KP, int RB>
+// time (128, the usual case), else 0.  M64: the offsets and masks are DCNv4's
+// merged 64-byte rows (P = 9, 16-bit; kp.merged_rows64), read whole (a
+// separate instance, so that the separate tensors' instance is unchanged).
+template <typename T, int CPT, int KP, int RB, bool M64 = false>
 __global__ void __launch_bounds__(256)
 fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, const TileGeom tg,
                 const T* __restrict__ input, const T* __restrict__ offset,
@@ -113,17 +115,14 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
   UnitRows<T, KP> rows;
   bool vec = false;
   constexpr bool kVecRows = KP > 0 && (sizeof(T) == 2 || CPT <= 8);
-  if constexpr (kVecRows) {
-    if (!kp.merged) {
-      vec = active && rows.load(offset, mask, kp.units, orow, mrow);
-    } else if constexpr (KP == 9 && sizeof(T) == 2) {
-      // DCNv4's merged 64-byte rows: the whole row in two 256-bit loads
-      if (active && kp.merged_rows64 &&
-          DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)) {
-        rows.load_merged64(orow);
-        vec = true;
-      }
+  if constexpr (M64) {
+    // DCNv4's merged 64-byte rows: the whole row in two 256-bit loads
+    if (active && DCN_IN_SPAN(orow, 64, offset, offset_bytes<T>(kp), kBadRow)) {
+      rows.load_merged64(orow);
+      vec = true;
     }
+  } else if constexpr (kVecRows) {
+    vec = active && !kp.merged && rows.load(offset, mask, kp.units, orow, mrow);
   }
 
   float mx = 0.f, inv = 1.f;
@@ -314,6 +313,10 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
     auto k = kp.P == 9 ? (r128 ? fwd_tile_kernel<T, CPT, 9, 128> : fwd_tile_kernel<T, CPT, 9, 0>)
            : kp.P == 8 ? (r128 ? fwd_tile_kernel<T, CPT, 8, 128> : fwd_tile_kernel<T, CPT, 8, 0>)
                        : (r128 ? fwd_tile_kernel<T, CPT, 0, 128> : fwd_tile_kernel<T, CPT, 0, 0>);
+    if constexpr (sizeof(T) == 2) {
+      if (kp.P == 9 && kp.merged && kp.merged_rows64)
+        k = r128 ? fwd_tile_kernel<T, CPT, 9, 128, true> : fwd_tile_kernel<T, CPT, 9, 0, true>;
+    }
     if (smem > 48 * 1024) {
       cudaError_t e =
           cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
