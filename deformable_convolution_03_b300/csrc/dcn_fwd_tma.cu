@@ -260,7 +260,7 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
 
 // ---- host side ------------------------------------------------------------------
 
-// The driver's tensor-map encoder, looked up once through the runtime (the
+// The CUDA driver's tensor-map encoder, looked up once through the runtime (the
 // library links the runtime only).
 static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

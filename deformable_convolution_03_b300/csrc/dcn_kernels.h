@@ -40,7 +40,7 @@ cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, in
 
 // The TMA-staged forward (dcn_fwd_tma.cu).  encode_input_map fills the
 // 128-byte tensor map of the input (dims C, W, H, N; box GB*gc x WW x WH x 1;
-// out-of-range elements read as zero) and returns false when the driver
+// out-of-range elements read as zero) and returns false when the CUDA driver
 // rejects it; launch_fwd_tile runs fwd_tile_kernel with cpt as the wide
 // forward's (16 to 64 bytes per slice) over the tiles of kp.
 bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const void* input,
@@ -50,8 +50,8 @@ cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& 
                             cudaStream_t s);
 // Blocks whose bounded wait for a tensor copy ran out, since load.
 cudaError_t read_wait_timeouts(unsigned long long* count);
-// The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000, to
-// be cast by the caller), or nullptr if the driver does not provide it.
+// The CUDA driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000,
+// to be cast by the caller), or nullptr if the CUDA driver does not provide it.
 void* tensor_map_encoder();
 
 // The forward with the merged offset/mask projection in its prologue

@@ -108,13 +108,13 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
              note="DCNv4 fwd+bwd, stride 2, pad 1, dilation 2"),
 ]}
 
-# The five configurations in order, by workload name.
-CONFIGS = {
-    1: ["v3_tiny_f32"],
-    2: ["t_stage1_f16"],
-    3: ["t_stage1_bf16", "t_stage2_bf16", "t_stage3_bf16", "t_stage4_bf16"],
-    4: ["g_stage1_bf16", "g_stage1_rc_bf16"],
-    5: ["fb28_f32", "fb28_s2d2_f32"],
+# The workloads grouped by what they exercise.
+SUITES = {
+    "dcnv3_tiny_f32": ["v3_tiny_f32"],
+    "dcnv4_t_stage1_f16": ["t_stage1_f16"],
+    "dcnv4_t_stages_bf16": ["t_stage1_bf16", "t_stage2_bf16", "t_stage3_bf16", "t_stage4_bf16"],
+    "dcnv3_g_stage1_bf16": ["g_stage1_bf16", "g_stage1_rc_bf16"],
+    "dcnv4_fwd_bwd_f32": ["fb28_f32", "fb28_s2d2_f32"],
 }
 
 # FlashInternImage-T block depths per stage (DEPTHS [4, 4, 18, 4]).

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from deformable_convolution_03_b300 import binding as B
-from deformable_convolution_03_b300.inputs import CONFIGS, WORKLOADS, Workload, make_inputs
+from deformable_convolution_03_b300.inputs import SUITES, WORKLOADS, Workload, make_inputs
 from parity import (assert_close, check_bwd, check_fwd, f64, lib_params, oracle_params, run_bwd,
                     run_fwd)
 
@@ -36,7 +36,7 @@ def small(name, dtype="f32", **kw) -> Workload:
 
 # ---- the five configurations at full size -------------------------------------
 
-ALL = [n for c in sorted(CONFIGS) for n in CONFIGS[c]]
+ALL = [n for suite in SUITES.values() for n in suite]
 
 
 @pytest.mark.parametrize("name", ALL)
@@ -45,13 +45,13 @@ def test_config_forward_full_size(name):
     check_fwd(w, make_inputs(w))
 
 
-@pytest.mark.parametrize("name", CONFIGS[5])
+@pytest.mark.parametrize("name", SUITES["dcnv4_fwd_bwd_f32"])
 def test_config_backward_full_size(name):
     w = WORKLOADS[name]
     check_bwd(w, make_inputs(w))
 
 
-BWD16 = CONFIGS[2] + CONFIGS[3] + CONFIGS[4]
+BWD16 = SUITES["dcnv4_t_stage1_f16"] + SUITES["dcnv4_t_stages_bf16"] + SUITES["dcnv3_g_stage1_bf16"]
 
 
 @pytest.mark.parametrize("name", BWD16)
