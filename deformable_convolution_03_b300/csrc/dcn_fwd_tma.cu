@@ -169,53 +169,62 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
     // after the loop, so that the unrolled loop holds only the shared-memory
     // path
     unsigned long long far = 0ull;
+    // the point loop, compiled once with the rows in registers (V) and once
+    // reading them from memory point by point
+    auto points = [&](auto rows_in_regs) {
+      constexpr bool V = decltype(rows_in_regs)::value;
 #pragma unroll(KP > 0 ? KP : 1)
-    for (int p = 0; p < P; ++p) {
-      float m;
-      float2 d;
-      if (KP > 0 && vec) {
-        m = rows.msk(KP > 0 ? p : 0);
-        d = rows.off(KP > 0 ? p : 0);
-      } else {
-        m = ld_once_1(mrow + p);
-        d = ld_once_2(orow + 2 * p);
-      }
-      if (kp.softmax) m = expf(m - mx) * inv;
-      const float x = location(d.x, kp.tap_x[p], scale, ref_x);
-      const float y = location(d.y, kp.tap_y[p], scale, ref_y);
-      if (!in_box(x, y, kp.W, kp.H)) continue;  // also NaN / inf
-      const float xf = floorf(x), yf = floorf(y);
-      const int cx = (int)xf - wx0, cy = (int)yf - wy0;
-      if (!(ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm)) {
-        far |= 1ull << p;
-        continue;
-      }
-      // the cell is in the window: corners from shared memory, zeros standing
-      // for pixels outside the image
-      const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
-      const float gym = gy * m, fym = fy * m;
-      const unsigned char* a00 = smem + (uint32_t)(cy * tg.WW + cx) * rb;
-      const uint32_t at[4] = {0u, rb, wrb, wrb + rb};  // the corners' offsets
-      const float w[4] = {gym * gx, gym * fx, fym * gx, fym * fx};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t v[NW];
-#pragma unroll
-        for (int j = 0; j < NC; ++j) {
-          // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
-          // plain loads, so that the compiler may fold constant offsets
-          const unsigned char* q = a00 + coff[j] + at[k];
-          const uint4 c = DCN_IN_SPAN(q, 16, smem, tg.win_bytes, kBadShared)
-                              ? *reinterpret_cast<const uint4*>(q)
-                              : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * j] = c.x;
-          v[4 * j + 1] = c.y;
-          v[4 * j + 2] = c.z;
-          v[4 * j + 3] = c.w;
+      for (int p = 0; p < P; ++p) {
+        float m;
+        float2 d;
+        if constexpr (KP > 0 && V) {
+          m = rows.msk(KP > 0 ? p : 0);
+          d = rows.off(KP > 0 ? p : 0);
+        } else {
+          m = ld_once_1(mrow + p);
+          d = ld_once_2(orow + 2 * p);
         }
-        fma_words<T, NW>(acc, v, Fma<T>::weight(w[k]));
+        if (kp.softmax) m = expf(m - mx) * inv;
+        const float x = location(d.x, kp.tap_x[p], scale, ref_x);
+        const float y = location(d.y, kp.tap_y[p], scale, ref_y);
+        if (!in_box(x, y, kp.W, kp.H)) continue;  // also NaN / inf
+        const float xf = floorf(x), yf = floorf(y);
+        const int cx = (int)xf - wx0, cy = (int)yf - wy0;
+        if (!(ready && (unsigned)cx < (unsigned)WWm && (unsigned)cy < (unsigned)WHm)) {
+          far |= 1ull << p;
+          continue;
+        }
+        // the cell is in the window: corners from shared memory, zeros standing
+        // for pixels outside the image
+        const float fx = x - xf, fy = y - yf, gx = 1.f - fx, gy = 1.f - fy;
+        const float gym = gy * m, fym = fy * m;
+        const unsigned char* a00 = smem + (uint32_t)(cy * tg.WW + cx) * rb;
+        const uint32_t at[4] = {0u, rb, wrb, wrb + rb};  // the corners' offsets
+        const float w[4] = {gym * gx, gym * fx, fym * gx, fym * fx};
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t v[NW];
+  #pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            // accumulator chunk j takes the slice's chunk (j + rot) mod NC;
+            // plain loads, so that the compiler may fold constant offsets
+            const unsigned char* q = a00 + coff[j] + at[k];
+            const uint4 c = DCN_IN_SPAN(q, 16, smem, tg.win_bytes, kBadShared)
+                                ? *reinterpret_cast<const uint4*>(q)
+                                : make_uint4(0u, 0u, 0u, 0u);
+            v[4 * j] = c.x;
+            v[4 * j + 1] = c.y;
+            v[4 * j + 2] = c.z;
+            v[4 * j + 3] = c.w;
+          }
+          fma_words<T, NW>(acc, v, Fma<T>::weight(w[k]));
+        }
       }
-    }
+    };
+    if (KP > 0 && vec)
+      points(std::true_type{});
+    else
+      points(std::false_type{});
     // far points: the point again, clamped corners from global memory,
     // weight 0 outside the image
     while (far) {
