@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "d57a24249f5e", "8f737ff9692f"
+_F, _B = "1f28482ee423", "fbd162be7626"
 TRAFFIC = {
-    "fwd@v3_tiny_f32": {"bytes": 47_872, "sha": _F},
+    "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_207_104, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 269_573_632, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_239_360, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_458_752, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_705_664, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_132_544, "sha": _B},
-    "fwd@t_stage3_bf16": {"bytes": 17_298_688, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 49_479_424, "sha": _B},
-    "fwd@t_stage4_bf16": {"bytes": 8_668_160, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 24_791_552, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_422_528, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 311_462_400, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_403_008, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_512_192, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 73_695_232, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_313_792, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_060_736, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_508_992, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_099_584, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_303_552, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_098_304, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_353_280, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_677_248, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_267_712, "sha": _B},
+    "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
+    "bwd@t_stage3_bf16": {"bytes": 23_805_696, "sha": _B},
+    "fwd@t_stage4_bf16": {"bytes": 8_687_104, "sha": _F},
+    "bwd@t_stage4_bf16": {"bytes": 11_939_072, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_679_552, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 310_952_192, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_361_536, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_160_192, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 74_155_008, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_413_888, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_612_160, "sha": _B},
 }
 
 
