@@ -277,12 +277,14 @@ class Case:
         return 2 + (1 if self.ws_bytes else 0)
 
 
-def timed_steps(case: Case, steps: int, flush: torch.Tensor, phases=("fwd", "bwd")):
-    """Per-step, per-phase device times (ms), each step after an L2 flush."""
+def timed_steps(case: Case, steps: int, flush, phases=("fwd", "bwd")):
+    """Per-step, per-phase device times (ms), each step after an L2 flush
+    (none when flush is None: the warm-cache reading)."""
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
           for _ in range(steps)]
     for k in range(steps):
-        flush.zero_()
+        if flush is not None:
+            flush.zero_()
         ev[k][0].record()
         for j, ph in enumerate(phases):
             getattr(case, ph)()
@@ -708,6 +710,14 @@ def main():
     bwd_ms = statistics.mean(t["bwd"])
     step_ms, fwd_ms, bwd_ms = max_over_ranks([fwd_ms + bwd_ms, fwd_ms, bwd_ms], dist, dev)
 
+    # secondary reading after the timed region: the same steps without the
+    # flush, so that what the previous step left in L2 is reused
+    warm_steps = min(args.steps, 200)
+    tw = timed_steps(case, warm_steps, None)
+    warm = {"fwd_median": round(statistics.median(tw["fwd"]), 5),
+            "bwd_median": round(statistics.median(tw["bwd"]), 5), "steps": warm_steps,
+            "how": "no L2 flush between steps (secondary; the headline flushes)"}
+
     ib = case.ideal()
     step_bytes = ib["fwd"] + ib["bwd"]
     value = aggregate_gbs(step_bytes, world, step_ms)
@@ -756,7 +766,9 @@ def main():
         "roofline_fwd": roof["fwd"],
         "phases_ms": {"fwd": round(fwd_ms, 5), "bwd": round(bwd_ms, 5),
                       "fwd_median": round(statistics.median(t["fwd"]), 5),
-                      "bwd_median": round(statistics.median(t["bwd"]), 5)},
+                      "bwd_median": round(statistics.median(t["bwd"]), 5),
+                      "fwd_min": round(min(t["fwd"]), 5), "bwd_min": round(min(t["bwd"]), 5),
+                      "warm_l2": warm},
         "ideal_bytes": {"fwd": ib["fwd"], "bwd": ib["bwd"]},
         "e2e": e2e,
         "gpu_launches": args.steps * case.launches_per_step(),
