@@ -524,13 +524,19 @@ __device__ __forceinline__ void input_block(const KParams& kp, const WinGeom& wg
   const int lane = threadIdx.x & 31;
   const int ry0 = max(0, -wy0), ry1 = min(wg.WH, H - wy0);
   const int rx0 = max(0, -wx0), rx1 = min(wg.WW, W - wx0);
-  const int cols = rx1 - rx0;
-  const int npix = cols > 0 && ry1 > ry0 ? (ry1 - ry0) * cols : 0;
+  const int cols = rx1 - rx0, rows = ry1 - ry0;
+  const int npix = cols > 0 && rows > 0 ? rows * cols : 0;
+  // A warp's consecutive pixels run along the region's longer side: visit
+  // counts fall off across the halo, and a line along the long side crosses
+  // fewer halo pixels (FlashInternImage-T stage 2's 43 x 22 windows: backward
+  // 164 -> 150 us against rows first).
+  const bool by_rows = cols >= rows;
+  const int line = by_rows ? cols : rows;
   for (int base = threadIdx.x - lane; base < npix; base += blockDim.x) {
     const int i = base + lane;
     const bool valid = i < npix;
-    const int qy = valid ? i / cols : 0;
-    const int ry = ry0 + qy, rx = rx0 + (valid ? i - qy * cols : 0);
+    const int across = valid ? i / line : 0, along = valid ? i - across * line : 0;
+    const int ry = ry0 + (by_rows ? across : along), rx = rx0 + (by_rows ? along : across);
     const int yy = wy0 + ry, xx = wx0 + rx;
     // the cells (cy, rx - 1) and (cy, rx) of cell rows cy = ry - 1 (range a,
     // the pixel is their lower corner) and cy = ry (range b, upper corner):
