@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "1f28482ee423", "fbd162be7626"
+_F, _B = "1f28482ee423", "de6346c2d667"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_099_584, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 269_303_552, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_098_304, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_353_280, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_677_248, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_267_712, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_335_360, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_349_120, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_082_688, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 269_003_008, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_630_144, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_202_944, "sha": _B},
     "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_805_696, "sha": _B},
-    "fwd@t_stage4_bf16": {"bytes": 8_687_104, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 11_939_072, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_679_552, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 310_952_192, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_361_536, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_160_192, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 74_155_008, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_413_888, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_612_160, "sha": _B},
+    "bwd@t_stage3_bf16": {"bytes": 23_811_584, "sha": _B},
+    "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
+    "bwd@t_stage4_bf16": {"bytes": 11_939_584, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_455_040, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 311_594_752, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_098_368, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_332_736, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 74_145_536, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_394_176, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_062_016, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_617_024, "sha": _B},
 }
 
 
@@ -443,7 +443,7 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
 
 
 def _time_alone(fn, flush, reps: int) -> float:
-    """Mean ms of fn over reps calls, each after an L2 flush, by CUDA events on
+    """Median ms of fn over reps calls, each after an L2 flush, by CUDA events on
     the current stream (three untimed calls first)."""
     for _ in range(3):
         fn()
@@ -456,7 +456,9 @@ def _time_alone(fn, flush, reps: int) -> float:
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
-    return statistics.mean(ts)
+    # the median: a call whose host-side wrapper outlasts the flush before it
+    # leaves the device idle between the first event and the kernel
+    return statistics.median(ts)
 
 
 def images_per_s(dev, flush, reps: int):
