@@ -376,8 +376,9 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     branch's feature step (dcn_dwconv_ln_gelu), on synthetic inputs and
     weights, each timed alone with L2 flushed, against HBM on their ideal
     bytes (each tensor read or written once); and the forward with its
-    projection in one launch (dcn_core_fwd_proj) beside the same work as two
-    launches."""
+    projection in one launch (dcn_core_fwd_proj), and the forward with the
+    centre feature scale in its epilogue (dcn_core_fwd_cfs), each beside the
+    same work as two launches."""
     dt = DTYPES[w.dtype]
     M, C = w.N * w.H_out * w.W_out, w.C
     rs = 32 if w.P == 9 else ((3 * w.P + 7) // 8) * 8
@@ -439,6 +440,27 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
         out["forward_with_projection"] = {
             "shape": f"{M}x{C} -> {w.G}x{rs} rows, then the core", "ms": round(fused, 5),
             "two_launches_ms": round(two, 5)}
+    # the core forward with the centre feature scale (x_proj = the core's
+    # input) in its epilogue, beside the core forward and the gate as two
+    # launches; ideal bytes: the core's plus the logits'
+    if w.H_out == w.H and w.W_out == w.W and w.stride_h == 1 and w.stride_w == 1:
+        p = B.Params(dtype=B.TORCH_TO_DCN[dt], **w.params())
+        t = {key: v.to(dev) for key, v in make_inputs(w).items()}
+        lgu = torch.randn(w.N, w.H_out, w.W_out, w.G, generator=g).to(dt).to(dev)
+        y = torch.empty(w.N, w.H_out, w.W_out, C, dtype=dt, device=dev)
+        fused = _time_alone(lambda: B.dcn_core_fwd_cfs(p, t["input"], t["offset"], t["mask"], lgu,
+                                                       y), flush, reps)
+        two = _time_alone(lambda: (B.dcn_core_fwd(p, t["input"], t["offset"], t["mask"], y),
+                                   B.dcn_center_feature_scale(y.reshape(M, C),
+                                                              t["input"].reshape(M, C),
+                                                              lgu.reshape(M, w.G), y.reshape(M, C),
+                                                              w.G)), flush, reps)
+        ideal = ideal_bytes(w)["fwd"] + M * w.G * es
+        gbs = ideal / (fused * 1e-3) / 1e9
+        out["forward_with_cfs"] = {"shape": f"{M} pixels x {w.G} gates, the core's workload",
+                                   "ms": round(fused, 5), "two_launches_ms": round(two, 5),
+                                   "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
+                                   "ideal_bytes": ideal}
     return out
 
 

@@ -33,7 +33,7 @@ DCN_MAX_POINTS = 64
 TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: DCN_BF16}
 
 # Every symbol include/dcn_core.h declares.
-EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om",
+EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om", "dcn_core_fwd_cfs",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
            "dcn_core_fwd_proj", "dcn_linear", "dcn_center_feature_scale",
            "dcn_center_feature_scale_bwd", "dcn_dwconv_ln_gelu", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
@@ -100,6 +100,7 @@ def _open(path: str) -> ctypes.CDLL:
     L.dcn_core_bwd.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
     L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
+    L.dcn_core_fwd_cfs.argtypes = [PP, vp, vp, vp, vp, vp, vp]
     L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
     L.dcn_core_fwd_proj.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp]
     L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
@@ -313,6 +314,14 @@ def dcn_core_fwd(p: Params, input, offset, mask, output, stream=None) -> None:
     """Raw entry point: pointers (tensors or ints) in, output written in place."""
     _check(lib().dcn_core_fwd(ctypes.byref(p.c()), _ptr(input), _ptr(offset), _ptr(mask),
                               _ptr(output), _stream(stream)), "dcn_core_fwd")
+
+
+def dcn_core_fwd_cfs(p: Params, input, offset, mask, logits, output, stream=None) -> None:
+    """Raw entry point: the core forward followed by the centre feature scale
+    with x_proj = input and logits (N, Ho, Wo, G); output written in place."""
+    _check(lib().dcn_core_fwd_cfs(ctypes.byref(p.c()), _ptr(input), _ptr(offset), _ptr(mask),
+                                  _ptr(logits), _ptr(output), _stream(stream)),
+           "dcn_core_fwd_cfs")
 
 
 def dcn_core_bwd_workspace(p: Params) -> int:

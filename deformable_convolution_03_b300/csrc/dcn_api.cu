@@ -456,20 +456,28 @@ int dcn_num_points(const dcn_params_t* p) {
 
 namespace {
 
+int cfs_vbytes(int gc, int es, bool bwd, std::initializer_list<const void*> ptrs);
+
 // Both layouts of the offsets and masks: separate tensors (row strides 2P and
 // P) or one merged tensor (offset row, then mask row, in rows of
-// row_stride elements).
+// row_stride elements).  cfs: the centre feature scale follows, with x_proj
+// the input and one logit per unit (an output the input's size, stride 1):
+// in the TMA forward's epilogue for 16-bit storage, else as a second launch
+// over the output in place.
 int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
-             void* output, void* stream, int row_stride) {
+             void* output, void* stream, int row_stride, bool cfs = false,
+             const void* logits = nullptr) {
   Geometry g;
   int rc = validate(p, &g);
   if (rc != DCN_OK) return rc;
   if (row_stride && (row_stride < 3 * g.P || row_stride % 2)) return DCN_ERR_SHAPE;
+  if (cfs && (p->stride_h != 1 || p->stride_w != 1 || g.Ho != p->H || g.Wo != p->W))
+    return DCN_ERR_SHAPE;
   if (g.units == 0) return DCN_OK;
-  if (!input || !offset || !mask || !output) return DCN_ERR_NULL;
+  if (!input || !offset || !mask || !output || (cfs && !logits)) return DCN_ERR_NULL;
   const size_t es = (size_t)elem_size(p->dtype);
   if (!aligned(input, es) || !aligned(mask, es) || !aligned(output, es) ||
-      !aligned(offset, 2 * es))
+      !aligned(offset, 2 * es) || (cfs && !aligned(logits, es)))
     return DCN_ERR_ALIGN;
   dcn::KParams kp;
   fill_kparams(p, g, &kp);
@@ -486,13 +494,19 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
                                              dcn::options().fwd_any_tile != 0);
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   if (fault_injected()) return DCN_ERR_CUDA;
-  if (tile)
-    return finish(cuda_status(dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset,
-                                                   mask, output, static_cast<cudaStream_t>(stream))),
-                  stream);
-  return finish(cuda_status(dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output,
-                                            static_cast<cudaStream_t>(stream))),
-                stream);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool fused = cfs && tile && es == 2 && !row_stride && dcn::options().fwd_cfs;
+  cudaError_t e =
+      tile ? dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset, mask, output, st,
+                                  fused ? logits : nullptr)
+           : dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output, st);
+  if (e == cudaSuccess && cfs && !fused) {
+    const int gc = p->gc;
+    e = dcn::launch_cfs_fwd(p->dtype, cfs_vbytes(gc, (int)es, false, {output, input, output}),
+                            (long long)p->N * g.Ho * g.Wo, p->G * gc, p->G, output, input, logits,
+                            output, st);
+  }
+  return finish(cuda_status(e), stream);
 }
 
 }  // namespace
@@ -502,6 +516,11 @@ extern "C" {
 int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
                  void* output, void* stream) {
   return core_fwd(p, input, offset, mask, output, stream, 0);
+}
+
+int dcn_core_fwd_cfs(const dcn_params_t* p, const void* input, const void* offset,
+                     const void* mask, const void* logits, void* output, void* stream) {
+  return core_fwd(p, input, offset, mask, output, stream, 0, true, logits);
 }
 
 int dcn_core_fwd_om(const dcn_params_t* p, const void* input, const void* offset_mask,
@@ -884,6 +903,7 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_halo", &dcn::Options::fwd_halo},
     {"fwd_any_tile", &dcn::Options::fwd_any_tile},
     {"fwd_row64", &dcn::Options::fwd_row64},
+    {"fwd_cfs", &dcn::Options::fwd_cfs},
     {"fwd_proj", &dcn::Options::fwd_proj},
     {"fwd_proj_win", &dcn::Options::fwd_proj_win},
     {"fwd_proj_ws", &dcn::Options::fwd_proj_ws},

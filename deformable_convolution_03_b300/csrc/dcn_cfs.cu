@@ -54,7 +54,7 @@ __device__ __forceinline__ void store_v(T* p, const float (&f)[V]) {
   *reinterpret_cast<Pack<T, V>*>(p) = k;
 }
 
-__device__ __forceinline__ float gate(float l) { return 1.f / (1.f + expf(-l)); }
+__device__ __forceinline__ float gate(float l) { return cfs_gate(l); }
 
 // One thread per chunk of V channels; V divides gc.  out may be core or x_proj
 // (each element is read and written by one thread, reads first).

@@ -112,6 +112,10 @@ __host__ __device__ inline size_t split_smem_bytes(const WinGeom& wg, int P, int
          (2 * ncell + 1 + 32) * sizeof(int);
 }
 
+// The centre feature scale's gate s = 1 / (1 + e^-l) in float32 (its
+// forward kernel and the core forward that applies it in its epilogue).
+__device__ __forceinline__ float cfs_gate(float l) { return 1.f / (1.f + expf(-l)); }
+
 // ---- asynchronous tensor copies (TMA) and their barrier --------------------
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

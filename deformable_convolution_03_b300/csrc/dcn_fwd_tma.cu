@@ -62,11 +62,16 @@ __device__ __forceinline__ void unrotate_acc_t(float (&acc)[CPT], int rot) {
 // time (128, the usual case), else 0.  M64: the offsets and masks are DCNv4's
 // merged 64-byte rows (P = 9, 16-bit; kp.merged_rows64), read whole (a
 // separate instance, so that the separate tensors' instance is unchanged).
-template <typename T, int CPT, int KP, int RB, bool M64 = false>
+// CFS: the centre feature scale applied before the store (an output the
+// input's size, stride 1): out = core * (1 - s) + x_proj * s with s the gate of
+// the unit's logit and x_proj the input at the output pixel, which lies in the
+// window at the zero-offset centre tap (a gate of 1 passes x_proj exactly).
+template <typename T, int CPT, int KP, int RB, bool M64 = false, bool CFS = false>
 __global__ void __launch_bounds__(256)
 fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, const TileGeom tg,
                 const T* __restrict__ input, const T* __restrict__ offset,
-                const T* __restrict__ mask, T* __restrict__ output) {
+                const T* __restrict__ mask, T* __restrict__ output,
+                const T* __restrict__ logits = nullptr) {
   constexpr int NW = CPT * (int)sizeof(T) / 4;  // 32-bit words per corner slice
   constexpr int NC = NW / 4;                    // 16-byte chunks per corner slice
   extern __shared__ __align__(128) unsigned char smem[];
@@ -260,6 +265,38 @@ fwd_tile_kernel(const __grid_constant__ CUtensorMap tmap, const KParams kp, cons
       fma_words<T, NW>(acc, v11, Fma<T>::weight(wy1v * wx1v));
     }
     unrotate_acc_t<CPT, T>(acc, rot);
+    if constexpr (CFS) {
+      // the gate of the unit's logit (logits (N, Ho, Wo, G): index = unit), and
+      // x_proj = the input at (ho, wo), this thread's channels: from the window
+      // (in natural chunk order), or from memory if the copy did not land
+      const float sg = cfs_gate(DCN_IN_SPAN(logits + unit, sizeof(T), logits,
+                                            (size_t)kp.units * sizeof(T), kBadRow)
+                                    ? Dt<T>::one(logits + unit)
+                                    : 0.f);
+      const int cy = ho - wy0, cx = wo - wx0;
+      uint32_t xw[NW];
+      if (ready && (unsigned)cy < (unsigned)tg.WH && (unsigned)cx < (unsigned)tg.WW) {
+        const unsigned char* q = smem + (uint32_t)(cy * tg.WW + cx) * rb + 16u * chunk0;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          const uint4 c = DCN_IN_SPAN(q + 16 * j, 16, smem, tg.win_bytes, kBadShared)
+                              ? *reinterpret_cast<const uint4*>(q + 16 * j)
+                              : make_uint4(0u, 0u, 0u, 0u);
+          xw[4 * j] = c.x;
+          xw[4 * j + 1] = c.y;
+          xw[4 * j + 2] = c.z;
+          xw[4 * j + 3] = c.w;
+        }
+      } else {
+        ldg_words_in<NW>(img + ((uint32_t)ho * WC + (uint32_t)wo * C), xw, input,
+                         input_bytes<T>(kp));
+      }
+      float xv[CPT];
+#pragma unroll
+      for (int i = 0; i < NW; ++i) Dt<T>::unpack(xw[i], xv + i * Dt<T>::kPerWord);
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) acc[i] = fmaf(sg, xv[i], (1.f - sg) * acc[i]);
+    }
     if (out_in(kp, output, output + (size_t)unit * kp.gc + c0, CPT))
       Slice<T, CPT>::store(output + (size_t)unit * kp.gc + c0, acc);
   }
@@ -314,7 +351,8 @@ bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const vo
 
 template <typename T, int CPT>
 static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, const TileGeom& tg,
-                                 const T* i_, const T* o_, const T* m_, T* y_, cudaStream_t s) {
+                                 const T* i_, const T* o_, const T* m_, T* y_, const T* l_,
+                                 cudaStream_t s) {
   constexpr int bytes = CPT * (int)sizeof(T);
   if constexpr (bytes >= 16 && bytes <= 64) {
     const size_t smem = tg.win_bytes + 16;  // the window, then the barrier
@@ -325,6 +363,16 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
     if constexpr (sizeof(T) == 2) {
       if (kp.P == 9 && kp.merged && kp.merged_rows64)
         k = r128 ? fwd_tile_kernel<T, CPT, 9, 128, true> : fwd_tile_kernel<T, CPT, 9, 0, true>;
+      // the centre feature scale in the epilogue (separate offset / mask tensors)
+      if (l_)
+        k = kp.P == 9 ? (r128 ? fwd_tile_kernel<T, CPT, 9, 128, false, true>
+                              : fwd_tile_kernel<T, CPT, 9, 0, false, true>)
+          : kp.P == 8 ? (r128 ? fwd_tile_kernel<T, CPT, 8, 128, false, true>
+                              : fwd_tile_kernel<T, CPT, 8, 0, false, true>)
+                      : (r128 ? fwd_tile_kernel<T, CPT, 0, 128, false, true>
+                              : fwd_tile_kernel<T, CPT, 0, 0, false, true>);
+    } else {
+      if (l_) return cudaErrorInvalidValue;
     }
     if (smem > 48 * 1024) {
       cudaError_t e =
@@ -337,7 +385,7 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
     // warps: 256 for the power-of-two tiles, fewer for tiles such as 7 x 7
     const int threads = (kp.tile_w * kp.tile_h * tg.GB * (kp.gc / CPT) + 31) / 32 * 32;
     if (threads > 256) return cudaErrorInvalidConfiguration;
-    k<<<(unsigned)grid, threads, smem, s>>>(map, kp, tg, i_, o_, m_, y_);
+    k<<<(unsigned)grid, threads, smem, s>>>(map, kp, tg, i_, o_, m_, y_, l_);
     return cudaGetLastError();
   } else {
     return cudaErrorInvalidValue;
@@ -347,27 +395,29 @@ static cudaError_t launch_tile_t(const CUtensorMap& map, const KParams& kp, cons
 template <typename T>
 static cudaError_t launch_tile_d(const CUtensorMap& map, const KParams& kp, const TileGeom& tg,
                                  int cpt, const void* in, const void* off, const void* msk,
-                                 void* out, cudaStream_t s) {
+                                 void* out, const void* logits, cudaStream_t s) {
   const T* i_ = static_cast<const T*>(in);
   const T* o_ = static_cast<const T*>(off);
   const T* m_ = static_cast<const T*>(msk);
+  const T* l_ = static_cast<const T*>(logits);
   T* y_ = static_cast<T*>(out);
   switch (cpt) {
-    case 4: return launch_tile_t<T, 4>(map, kp, tg, i_, o_, m_, y_, s);
-    case 8: return launch_tile_t<T, 8>(map, kp, tg, i_, o_, m_, y_, s);
-    case 16: return launch_tile_t<T, 16>(map, kp, tg, i_, o_, m_, y_, s);
+    case 4: return launch_tile_t<T, 4>(map, kp, tg, i_, o_, m_, y_, l_, s);
+    case 8: return launch_tile_t<T, 8>(map, kp, tg, i_, o_, m_, y_, l_, s);
+    case 16: return launch_tile_t<T, 16>(map, kp, tg, i_, o_, m_, y_, l_, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& tg, int dtype,
                             int cpt, const void* in, const void* off, const void* msk, void* out,
-                            cudaStream_t s) {
+                            cudaStream_t s, const void* logits) {
   const CUtensorMap& m = *static_cast<const CUtensorMap*>(map);
   switch (dtype) {
-    case DCN_F32: return launch_tile_d<float>(m, kp, tg, cpt, in, off, msk, out, s);
-    case DCN_F16: return launch_tile_d<__half>(m, kp, tg, cpt, in, off, msk, out, s);
-    case DCN_BF16: return launch_tile_d<__nv_bfloat16>(m, kp, tg, cpt, in, off, msk, out, s);
+    case DCN_F32: return launch_tile_d<float>(m, kp, tg, cpt, in, off, msk, out, logits, s);
+    case DCN_F16: return launch_tile_d<__half>(m, kp, tg, cpt, in, off, msk, out, logits, s);
+    case DCN_BF16:
+      return launch_tile_d<__nv_bfloat16>(m, kp, tg, cpt, in, off, msk, out, logits, s);
     default: return cudaErrorInvalidValue;
   }
 }

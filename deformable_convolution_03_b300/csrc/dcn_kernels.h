@@ -45,9 +45,12 @@ cudaError_t launch_bwd_split(const KParams& kp, const WinGeom& wg, int dtype, in
 // forward's (16 to 64 bytes per slice) over the tiles of kp.
 bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const void* input,
                       void* map_out);
+// With logits (16-bit storage, separate offset / mask tensors, an output the
+// input's size at stride 1), the centre feature scale is applied before the
+// store (the fwd_tile_kernel CFS instance); cudaErrorInvalidValue otherwise.
 cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& tg, int dtype,
                             int cpt, const void* in, const void* off, const void* msk, void* out,
-                            cudaStream_t s);
+                            cudaStream_t s, const void* logits = nullptr);
 // Blocks whose bounded wait for a tensor copy ran out, since load.
 cudaError_t read_wait_timeouts(unsigned long long* count);
 // The CUDA driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000,

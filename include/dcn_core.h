@@ -293,6 +293,28 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
                                  void* grad_core, void* grad_x_proj, void* grad_logits,
                                  void* stream);
 
+/* The core op followed by the centre feature scale in one call, x_proj being
+ * the core's own input (the two sections cited above dcn_core_fwd and
+ * dcn_center_feature_scale): per (pixel, group) unit,
+ *     out = core * (1 - s) + input[n, ho, wo, g, :] * s,  s = 1 / (1 + exp(-logit)),
+ * which needs an output the input's size: stride 1 and padding
+ * dilation * (kernel - 1) / 2 on both axes (H_out == H, W_out == W).
+ *   input, offset, mask   as dcn_core_fwd
+ *   logits                (N, H_out, W_out, G), one per unit, read
+ *   output                (N, H_out, W_out, G*gc), fully overwritten; must not
+ *                         overlap the other tensors
+ * For float16 / bfloat16 with separate offset / mask tensors and the input
+ * laid out for the tensor-copy forward, one launch: the gate is applied to the
+ * core's float32 sums before their one rounding, with x_proj read from the
+ * block's staged input window.  Otherwise (float32, other layouts) two
+ * launches, dcn_core_fwd into output and dcn_center_feature_scale over it in
+ * place, whose core is rounded to the storage type first; the two ways agree
+ * within that one extra rounding.
+ * Errors as dcn_core_fwd, plus DCN_ERR_SHAPE when the output is not the
+ * input's size, DCN_ERR_NULL / DCN_ERR_ALIGN for logits. */
+int dcn_core_fwd_cfs(const dcn_params_t* p, const void* input, const void* offset,
+                     const void* mask, const void* logits, void* output, void* stream);
+
 /* The feature step of the DCN module's offset branch (page
  * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
  * item 2: the control features x1 from which the offset and mask projections

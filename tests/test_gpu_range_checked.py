@@ -62,6 +62,23 @@ def test_backward_checked(checked, w, mode, opts):
     assert _status(checked) == 0
 
 
+@pytest.mark.parametrize("fused", [1, 0])
+@pytest.mark.parametrize("w", [P.small("cfs_chk_f16", "f16", gc=16, G=4, N=2, H=13, W=11,
+                                       offset_std=3.0),
+                               P.small("cfs_chk_bf16", "bf16", gc=32, G=2, N=2, H=9, W=14,
+                                       softmax=1, remove_center=1, kernel_h=3, kernel_w=3)],
+                         ids=lambda w: w.name)
+def test_forward_with_centre_feature_scale_checked(checked, w, fused, opts):
+    # the gate in the forward's epilogue (x_proj from the staged window) and
+    # the two-launch path, against the oracle's composition
+    import test_gpu_fused_cfs as F
+    opts.set("fwd_cfs", fused)
+    t = make_inputs(w)
+    logits = F._logits(w)
+    assert_close(F._run(w, t, logits), F._expect(w, t, logits), w.dtype, w.name)
+    assert _status(checked) == 0
+
+
 @pytest.mark.parametrize("name", ["t_stage1_f16", "g_stage1_bf16", "fb28_s2d2_f32"])
 def test_stage_geometry_checked(checked, name):
     # two images at a configuration's plane size, channels and groups: the
