@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "1f28482ee423", "de6346c2d667"
+_F, _B = "c88ca4ec49f2", "66df8a6ad668"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
-    "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_335_360, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 269_349_120, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_082_688, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 269_003_008, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_630_144, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_202_944, "sha": _B},
+    "bwd@v3_tiny_f32": {"bytes": 51_712, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_250_880, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_210_368, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_071_936, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_917_248, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_630_656, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_202_688, "sha": _B},
     "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_811_584, "sha": _B},
+    "bwd@t_stage3_bf16": {"bytes": 23_831_808, "sha": _B},
     "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
     "bwd@t_stage4_bf16": {"bytes": 11_939_584, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_455_040, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 311_594_752, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_098_368, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_332_736, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 74_145_536, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_394_176, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_062_016, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_617_024, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_448_384, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 311_459_584, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_172_864, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_586_688, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 73_413_120, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_297_152, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_064_320, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_678_208, "sha": _B},
 }
 
 
@@ -374,8 +374,10 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     the output projection (C -> C) by dcn_linear, the centre feature scale's
     mix (dcn_center_feature_scale, forward and backward) and the offset
     branch's feature step (dcn_dwconv_ln_gelu), on synthetic inputs and
-    weights, each timed alone with L2 flushed, against HBM on their ideal
-    bytes (each tensor read or written once); and the forward with its
+    weights, each timed alone with L2 flushed (outputs allocated beforehand,
+    so that a call's host side stays shorter than the flush before it),
+    against HBM on their ideal bytes (each tensor read or written once); and
+    the forward with its
     projection in one launch (dcn_core_fwd_proj), and the forward with the
     centre feature scale in its epilogue (dcn_core_fwd_cfs), each beside the
     same work as two launches."""
@@ -388,7 +390,8 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
         x = (torch.rand(M, C, generator=g) * 2 - 1).to(dt).to(dev)
         wt = (torch.randn(n_out, C, generator=g) / C ** 0.5).to(dt).to(dev)
         b = torch.randn(n_out, generator=g).to(dt).to(dev)
-        ms = _time_alone(lambda: B.linear(x, wt, b), flush, reps)
+        y = torch.empty(M, n_out, dtype=dt, device=dev)
+        ms = _time_alone(lambda: B.dcn_linear(x, wt, b, y), flush, reps)
         es = torch.empty(0, dtype=dt).element_size()
         ideal = (M * C + n_out * C + n_out + M * n_out) * es
         gbs = ideal / (ms * 1e-3) / 1e9
@@ -399,10 +402,12 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     es = torch.empty(0, dtype=dt).element_size()
     core, xp, go = ((torch.rand(M, C, generator=g) * 2 - 1).to(dt).to(dev) for _ in range(3))
     lg = torch.randn(M, w.G, generator=g).to(dt).to(dev)
+    o1, o2, o3 = (torch.empty_like(core) for _ in range(3))
+    ol = torch.empty_like(lg)
     gates = {
-        "cfs_forward": (lambda: B.center_feature_scale(core, xp, lg),
+        "cfs_forward": (lambda: B.dcn_center_feature_scale(core, xp, lg, o1, w.G),
                         (3 * M * C + M * w.G) * es),
-        "cfs_backward": (lambda: B.center_feature_scale_backward(go, core, xp, lg),
+        "cfs_backward": (lambda: B.dcn_center_feature_scale_bwd(go, core, xp, lg, o2, o3, ol, w.G),
                          (5 * M * C + 2 * M * w.G) * es),
     }
     for name, (fn, ideal) in gates.items():
@@ -415,8 +420,9 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     t = make_dwconv_inputs(w.N, w.H, w.W, C, DW_KERNEL, w.dtype, seed=78)
     t = {key: v.to(dev) for key, v in t.items()}
     ideal = (2 * w.N * w.H * w.W * C + (DW_KERNEL ** 2 + 3) * C) * es
-    ms = _time_alone(lambda: B.dwconv_ln_gelu(t["x"], t["weight"], t["bias"], t["gamma"],
-                                              t["beta"]), flush, reps)
+    x1 = torch.empty_like(t["x"])
+    ms = _time_alone(lambda: B.dcn_dwconv_ln_gelu(t["x"], t["weight"], t["bias"], t["gamma"],
+                                                  t["beta"], x1, 1e-6), flush, reps)
     gbs = ideal / (ms * 1e-3) / 1e9
     out["dwconv_ln_gelu"] = {"shape": f"{w.N}x{w.H}x{w.W}x{C}, k{DW_KERNEL}", "ms": round(ms, 5),
                              "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
@@ -466,21 +472,21 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
 
 def _time_alone(fn, flush, reps: int) -> float:
     """Median ms of fn over reps calls, each after an L2 flush, by CUDA events on
-    the current stream (three untimed calls first)."""
+    the current stream (three untimed calls first).  All reps are queued before
+    one synchronisation, as the timed steps are, so that the device always has
+    the next flush and call waiting and a slow host moment is not timed."""
     for _ in range(3):
         fn()
-    ts = []
-    for _ in range(reps):
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    for e0, e1 in ev:
         flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
         e1.record()
-        torch.cuda.synchronize()
-        ts.append(e0.elapsed_time(e1))
-    # the median: a call whose host-side wrapper outlasts the flush before it
-    # leaves the device idle between the first event and the kernel
-    return statistics.median(ts)
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 def images_per_s(dev, flush, reps: int):
