@@ -388,7 +388,9 @@ int plan_split(const dcn_params_t* p, const Geometry& g, const void* in, const v
     *la = 2 * g.P;
     *lb = g.P;
   }
-  if (!dcn::options().bwd_stage || (size_t)ub * (*la + *lb) * es > kStageSmem) *la = *lb = 0;
+  if (!dcn::options().bwd_stage ||
+      (size_t)ub * (dcn::stage_stride(*la, es) + *lb) * es > kStageSmem)
+    *la = *lb = 0;
   return cpt;
 }
 

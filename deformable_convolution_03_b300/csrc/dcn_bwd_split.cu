@@ -160,8 +160,9 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
   const int lu = threadIdx.x / chunks;
   const int ub = blockDim.x / chunks;
   T* s_rows = reinterpret_cast<T*>(smem);
-  T* ro = la > 0 ? s_rows + lu * la : goff + (size_t)unit * kp.os_off;
-  T* rm = la > 0 ? (kp.merged ? ro + 2 * P : s_rows + ub * la + lu * lb)
+  const int ls = stage_stride(la, (int)sizeof(T));  // the offset rows' staging stride
+  T* ro = la > 0 ? s_rows + lu * ls : goff + (size_t)unit * kp.os_off;
+  T* rm = la > 0 ? (kp.merged ? ro + 2 * P : s_rows + ub * ls + lu * lb)
                  : gmask + (size_t)unit * kp.os_mask;
 
   float gm_row[KP > 0 ? KP : DCN_MAX_POINTS];
@@ -261,17 +262,23 @@ __device__ __forceinline__ void sample_block(const KParams& kp, const T* __restr
       if (hh >= kp.Ho) break;
       const size_t u0 = (((size_t)n * kp.Ho + hh) * kp.Wo + wo0) * kp.G;
       const int cnt = nw * kp.G, l0 = ty * kp.tile_w * kp.G;
-      warp_copy_out(goff + u0 * kp.os_off, s_rows + l0 * la, cnt * la * es, lane);
+      if (ls == la)
+        warp_copy_out(goff + u0 * kp.os_off, s_rows + l0 * la, cnt * la * es, lane);
+      else
+        warp_copy_rows_out(goff + u0 * kp.os_off, s_rows + l0 * ls, cnt, la * es, ls * es, lane);
       if (lb > 0)
-        warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * la + l0 * lb, cnt * lb * es, lane);
+        warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * ls + l0 * lb, cnt * lb * es, lane);
     }
   } else {
     const long long u0 = (long long)bid * ub;
     const int cnt = (int)min((long long)ub, kp.units - u0);
     if (cnt > 0 && warp == 0) {
-      warp_copy_out(goff + u0 * kp.os_off, s_rows, cnt * la * es, lane);
+      if (ls == la)
+        warp_copy_out(goff + u0 * kp.os_off, s_rows, cnt * la * es, lane);
+      else
+        warp_copy_rows_out(goff + u0 * kp.os_off, s_rows, cnt, la * es, ls * es, lane);
     } else if (cnt > 0 && warp == 1 && lb > 0) {
-      warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * la, cnt * lb * es, lane);
+      warp_copy_out(gmask + u0 * kp.os_mask, s_rows + ub * ls, cnt * lb * es, lane);
     }
   }
 }
@@ -752,7 +759,8 @@ static cudaError_t launch_sample_t(const KParams& kp, const T* go_, const T* i_,
     const long long grid = kp.tile_w > 0 ? (long long)kp.N * kp.tiles_w * kp.tiles_h
                                          : (kp.units * chunks + block - 1) / block;
     if (grid > INT_MAX) return cudaErrorInvalidConfiguration;
-    const size_t smem = la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0;
+    const size_t smem =
+        la > 0 ? (size_t)(block / chunks) * (stage_stride(la, sizeof(T)) + lb) * sizeof(T) : 0;
     auto k9 = bwd_sample_kernel<T, CPT, 9>;
     auto k8 = bwd_sample_kernel<T, CPT, 8>;
     auto k0 = bwd_sample_kernel<T, CPT, 0>;
@@ -802,7 +810,8 @@ static cudaError_t launch_both_t(const KParams& kp, const WinGeom& wg, const T* 
                                      : (kp.units * chunks + block - 1) / block;
   const long long nb = (long long)kp.N * kp.G * wg.tiles_h * wg.tiles_w;
   if (na + nb > INT_MAX) return cudaErrorInvalidConfiguration;
-  const size_t sa = la > 0 ? (size_t)(block / chunks) * (la + lb) * sizeof(T) : 0;
+  const size_t sa =
+      la > 0 ? (size_t)(block / chunks) * (stage_stride(la, sizeof(T)) + lb) * sizeof(T) : 0;
   const size_t sb = split_smem_bytes(wg, kp.P, kp.gc, (int)sizeof(T));
   const size_t smem = sa > sb ? sa : sb;
   auto k = kp.P == 9 ? bwd_both_kernel<T, CPT, NW, 9>

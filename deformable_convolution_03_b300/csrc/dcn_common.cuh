@@ -722,6 +722,39 @@ __device__ __forceinline__ void fma_words(float* acc, const uint32_t (&v)[NW], t
   }
 }
 
+// The shared-memory stride (elements of es bytes) of gradient rows of la
+// elements staged one unit per lane: a row of an even number of 32-bit words
+// gets one more word, so that consecutive lanes' rows start in different
+// banks (64-byte merged rows otherwise put every second lane's store in the
+// same bank).
+__host__ __device__ inline int stage_stride(int la, int es) {
+  return (la * es) % 4 == 0 && ((la * es) / 4) % 2 == 0 ? la + 4 / es : la;
+}
+
+// Copy `rows` rows of `row_bytes` (even) from shared memory rows `src_stride`
+// bytes apart (even) to contiguous global memory over the lanes of one warp,
+// in 32-bit words when the destination, the rows and the stride allow it,
+// else in 16-bit halves.
+template <typename U>
+__device__ __forceinline__ void copy_rows_by(U* d, const U* s, int rows, int per_row, int stride,
+                                             int lane) {
+  for (int i = lane; i < rows * per_row; i += 32) {
+    const int r = i / per_row;
+    d[i] = s[r * stride + (i - r * per_row)];
+  }
+}
+__device__ __forceinline__ void warp_copy_rows_out(void* dst, const void* src, int rows,
+                                                   int row_bytes, int src_stride, int lane) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) |
+                      static_cast<uintptr_t>(row_bytes) | static_cast<uintptr_t>(src_stride);
+  if ((a & 3) == 0)
+    copy_rows_by(static_cast<uint32_t*>(dst), static_cast<const uint32_t*>(src), rows,
+                 row_bytes / 4, src_stride / 4, lane);
+  else
+    copy_rows_by(static_cast<unsigned short*>(dst), static_cast<const unsigned short*>(src), rows,
+                 row_bytes / 2, src_stride / 2, lane);
+}
+
 // Copy `bytes` (even) from shared to global memory with the lanes of one warp,
 // in 16-byte pieces when both ends and the length allow it.
 __device__ __forceinline__ void warp_copy_out(void* dst, const void* src, int bytes, int lane) {
