@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "c88ca4ec49f2", "66df8a6ad668"
+_F, _B = "28f1ee3738c6", "1cd53b7f8042"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
-    "bwd@v3_tiny_f32": {"bytes": 51_712, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_250_880, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 269_210_368, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_071_936, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_917_248, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_630_656, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_202_688, "sha": _B},
+    "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_225_792, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 268_649_472, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_047_104, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_328_960, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_693_888, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_114_880, "sha": _B},
     "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_831_808, "sha": _B},
+    "bwd@t_stage3_bf16": {"bytes": 23_808_000, "sha": _B},
     "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 11_939_584, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_448_384, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 311_459_584, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_172_864, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_586_688, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 73_413_120, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_297_152, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_064_320, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_678_208, "sha": _B},
+    "bwd@t_stage4_bf16": {"bytes": 11_940_864, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_617_088, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 311_134_720, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_113_728, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_681_920, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 73_451_776, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_325_824, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_599_360, "sha": _B},
 }
 
 
