@@ -310,6 +310,10 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
  * launches, dcn_core_fwd into output and dcn_center_feature_scale over it in
  * place, whose core is rounded to the storage type first; the two ways agree
  * within that one extra rounding.
+ * The pre-gate core output is never materialised, so this is the inference
+ * form: the gate's backward (dcn_center_feature_scale_bwd) needs that core
+ * output, which a training step gets from dcn_core_fwd followed by
+ * dcn_center_feature_scale.
  * Errors as dcn_core_fwd, plus DCN_ERR_SHAPE when the output is not the
  * input's size, DCN_ERR_NULL / DCN_ERR_ALIGN for logits. */
 int dcn_core_fwd_cfs(const dcn_params_t* p, const void* input, const void* offset,
