@@ -9,6 +9,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_addoption(parser):
+    parser.addoption("--range-checked", action="store_true", default=False,
+                     help="run every test on the range-checked library (-DDCN_DEBUG_BOUNDS) "
+                          "instead of the normal one: any access outside its tensor makes the "
+                          "call return DCN_ERR_INTERNAL")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
 
@@ -21,10 +28,17 @@ def oracle_lib():
 
 
 @pytest.fixture(scope="session")
-def native():
-    """The CUDA library's binding, with the library built in-tree."""
+def native(request):
+    """The CUDA library's binding, with the library built in-tree (the
+    range-checked one under --range-checked)."""
     from deformable_convolution_03_b300 import build, binding
     build.build()
+    if request.config.getoption("--range-checked"):
+        binding.LIB_PATH = build.build(debug_bounds=True)
+        binding._lib = None
+        L = binding.lib()
+        L.dcn_internal_debug_bounds.restype = ctypes.c_int
+        assert L.dcn_internal_debug_bounds() == 1
     return binding
 
 

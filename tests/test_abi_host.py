@@ -299,7 +299,7 @@ def test_dwconv_argument_errors(native, opts):
 
 # ---- the range-checked build ---------------------------------------------------
 
-def test_range_checked_build_exports_every_declared_symbol(native):
+def test_range_checked_build_exports_every_declared_symbol(native, request):
     from deformable_convolution_03_b300 import build
     path = build.build(debug_bounds=True)
     with native.using_library(path) as L:
@@ -307,6 +307,8 @@ def test_range_checked_build_exports_every_declared_symbol(native):
             assert hasattr(L, n), n
         L.dcn_internal_debug_bounds.restype = ctypes.c_int
         assert L.dcn_internal_debug_bounds() == 1
+    # the session's library: the normal one, or the range-checked one when the
+    # whole suite runs on it (--range-checked)
     L = native.lib()
     L.dcn_internal_debug_bounds.restype = ctypes.c_int
-    assert L.dcn_internal_debug_bounds() == 0
+    assert L.dcn_internal_debug_bounds() == (1 if request.config.getoption("--range-checked") else 0)
