@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "28f1ee3738c6", "1cd53b7f8042"
+_F, _B = "546140b8b796", "b9205b6706d6"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_225_792, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 268_649_472, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_047_104, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_328_960, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_693_888, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_114_880, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_132_096, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_152_000, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_208_640, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_558_080, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_631_168, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_245_696, "sha": _B},
     "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_808_000, "sha": _B},
+    "bwd@t_stage3_bf16": {"bytes": 23_836_928, "sha": _B},
     "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
     "bwd@t_stage4_bf16": {"bytes": 11_940_864, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_617_088, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 311_134_720, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_113_728, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_681_920, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 73_451_776, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_325_824, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_599_360, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_715_904, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 311_057_920, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 63_263_232, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 301_410_816, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 73_114_624, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_196_544, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_064_320, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_596_544, "sha": _B},
 }
 
 
@@ -379,8 +379,9 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
     against HBM on their ideal bytes (each tensor read or written once); and
     the forward with its
     projection in one launch (dcn_core_fwd_proj), and the forward with the
-    centre feature scale in its epilogue (dcn_core_fwd_cfs), each beside the
-    same work as two launches."""
+    centre feature scale in its epilogue (dcn_core_fwd_cfs), and the forward
+    with the output projection in its epilogue (dcn_core_fwd_out), each beside
+    the same work as separate launches."""
     dt = DTYPES[w.dtype]
     M, C = w.N * w.H_out * w.W_out, w.C
     rs = 32 if w.P == 9 else ((3 * w.P + 7) // 8) * 8
@@ -467,6 +468,37 @@ def projections(w: Workload, dev, flush, reps: int, peak: float) -> dict:
                                    "ms": round(fused, 5), "two_launches_ms": round(two, 5),
                                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
                                    "ideal_bytes": ideal}
+    # the core forward with the output projection (C -> C, then the bias) in
+    # its epilogue, after the centre feature scale where the output keeps the
+    # input's size, beside the same work as launches of their own (the core,
+    # the gate, dcn_linear); ideal bytes: the core's with y for its output,
+    # plus the weight, the bias and the logits
+    if es == 2 and C == 64:
+        p = B.Params(dtype=B.TORCH_TO_DCN[dt], **w.params())
+        t = {key: v.to(dev) for key, v in make_inputs(w).items()}
+        same = w.H_out == w.H and w.W_out == w.W and w.stride_h == 1 and w.stride_w == 1
+        lgu = torch.randn(w.N, w.H_out, w.W_out, w.G, generator=g).to(dt).to(dev) if same else None
+        wt = (torch.randn(C, C, generator=g) / C ** 0.5).to(dt).to(dev)
+        bo = torch.randn(C, generator=g).to(dt).to(dev)
+        core = torch.empty(w.N, w.H_out, w.W_out, C, dtype=dt, device=dev)
+        y = torch.empty_like(core)
+        fused = _time_alone(lambda: B.dcn_core_fwd_out(p, t["input"], t["offset"], t["mask"], lgu,
+                                                       wt, bo, y), flush, reps)
+
+        def two():
+            if same:
+                B.dcn_core_fwd_cfs(p, t["input"], t["offset"], t["mask"], lgu, core)
+            else:
+                B.dcn_core_fwd(p, t["input"], t["offset"], t["mask"], core)
+            B.dcn_linear(core.reshape(M, C), wt, bo, y.reshape(M, C))
+
+        sep = _time_alone(two, flush, reps)
+        ideal = ideal_bytes(w)["fwd"] + (C * C + C + (M * w.G if same else 0)) * es
+        gbs = ideal / (fused * 1e-3) / 1e9
+        out["forward_with_output_projection"] = {
+            "shape": f"{M} pixels, {C} -> {C}" + (f", {w.G} gates first" if same else ""),
+            "ms": round(fused, 5), "two_launches_ms": round(sep, 5), "GB/s": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 4), "ideal_bytes": ideal}
     return out
 
 
@@ -615,8 +647,10 @@ def profile_proj(dev) -> int:
     scale forward and backward at stage 1 (200704 x 64, 4 gates, float16), and
     the offset branch's feature step (5 x 5 depthwise convolution, LayerNorm,
     GELU) at T stage 1 (64 x 56 x 56 x 64, float16) and G stage 1
-    (2 x 128 x 128 x 512, bfloat16), and the forward with its offset/mask
-    projection in one launch at T stage 1 (64 -> 4 x 32 rows, float16)."""
+    (2 x 128 x 128 x 512, bfloat16), and at T stage 1 in float16 the forward
+    with its offset/mask projection in one launch (64 -> 4 x 32 rows), with the
+    centre feature scale in its epilogue, and with the gate and the output
+    projection (64 -> 64) in its epilogue."""
     g = torch.Generator().manual_seed(1)
     calls = []
     for M, K, N, dt in ((200704, 64, 128, torch.float16), (200704, 64, 64, torch.float16),
@@ -644,6 +678,17 @@ def profile_proj(dev) -> int:
     bo = torch.randn(w.G * 32, generator=g).half().to(dev)
     y = torch.empty(w.N, w.H_out, w.W_out, w.C, dtype=torch.float16, device=dev)
     calls.append(lambda: B.dcn_core_fwd_proj(p, inp, feat, wt, bo, 32, y, None))
+    # the forward with the centre feature scale in its epilogue, and with the
+    # gate and then the output projection (64 -> 64) in its epilogue, stage 1
+    t = {key: v.to(dev) for key, v in make_inputs(w).items()}
+    lgu = torch.randn(w.N, w.H_out, w.W_out, w.G, generator=g).half().to(dev)
+    wo = (torch.randn(64, 64, generator=g) / 8).half().to(dev)
+    bw = torch.randn(64, generator=g).half().to(dev)
+    yc = torch.empty_like(y)
+    yo = torch.empty_like(y)
+    calls.append(lambda: B.dcn_core_fwd_cfs(p, t["input"], t["offset"], t["mask"], lgu, yc))
+    calls.append(lambda: B.dcn_core_fwd_out(p, t["input"], t["offset"], t["mask"], lgu, wo, bw,
+                                            yo))
     for f in calls:
         f()
         f()

@@ -34,6 +34,7 @@ TORCH_TO_DCN = {torch.float32: DCN_F32, torch.float16: DCN_F16, torch.bfloat16: 
 
 # Every symbol include/dcn_core.h declares.
 EXPORTS = ("dcn_out_shape", "dcn_num_points", "dcn_core_fwd", "dcn_core_fwd_om", "dcn_core_fwd_cfs",
+           "dcn_core_fwd_out",
            "dcn_core_bwd_workspace", "dcn_core_bwd", "dcn_core_bwd_om", "dcn_core_bwd_noalloc",
            "dcn_core_fwd_proj", "dcn_linear", "dcn_center_feature_scale",
            "dcn_center_feature_scale_bwd", "dcn_dwconv_ln_gelu", "dcn_wait_timeouts", "dcn_status_str", "dcn_version")
@@ -101,6 +102,7 @@ def _open(path: str) -> ctypes.CDLL:
     L.dcn_core_bwd_noalloc.argtypes = [PP, vp, vp, vp, vp, vp, vp, vp, vp]
     L.dcn_core_fwd_om.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp]
     L.dcn_core_fwd_cfs.argtypes = [PP, vp, vp, vp, vp, vp, vp]
+    L.dcn_core_fwd_out.argtypes = [PP, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp]
     L.dcn_core_bwd_om.argtypes = [PP, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
     L.dcn_core_fwd_proj.argtypes = [PP, vp, vp, ctypes.c_int, vp, vp, ctypes.c_int, vp, vp, vp]
     L.dcn_wait_timeouts.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
@@ -322,6 +324,17 @@ def dcn_core_fwd_cfs(p: Params, input, offset, mask, logits, output, stream=None
     _check(lib().dcn_core_fwd_cfs(ctypes.byref(p.c()), _ptr(input), _ptr(offset), _ptr(mask),
                                   _ptr(logits), _ptr(output), _stream(stream)),
            "dcn_core_fwd_cfs")
+
+
+def dcn_core_fwd_out(p: Params, input, offset, mask, logits, weight, bias, y, scratch=None,
+                     stream=None) -> None:
+    """Raw entry point: the core forward (with the centre feature scale when
+    logits is given) followed by the output projection y = out weight^T + bias;
+    scratch (N, Ho, Wo, C) is needed only where the single launch does not apply."""
+    _check(lib().dcn_core_fwd_out(ctypes.byref(p.c()), _ptr(input), _ptr(offset), _ptr(mask),
+                                  _ptr(logits), _ptr(weight), _ptr(bias), int(weight.shape[0]),
+                                  _ptr(y), _ptr(scratch), _stream(stream)),
+           "dcn_core_fwd_out")
 
 
 def dcn_core_bwd_workspace(p: Params) -> int:

@@ -460,26 +460,40 @@ namespace {
 
 int cfs_vbytes(int gc, int es, bool bwd, std::initializer_list<const void*> ptrs);
 
+// The output projection after the core: y (N, Ho, Wo, n_out) = out w^T + bias.
+struct OutArgs {
+  const void* w;
+  const void* bias;
+  int n_out;
+  void* y;
+};
+
 // Both layouts of the offsets and masks: separate tensors (row strides 2P and
 // P) or one merged tensor (offset row, then mask row, in rows of
 // row_stride elements).  cfs: the centre feature scale follows, with x_proj
 // the input and one logit per unit (an output the input's size, stride 1):
 // in the TMA forward's epilogue for 16-bit storage, else as a second launch
-// over the output in place.
+// over the output in place.  oa: the output projection follows, in the TMA
+// forward's epilogue where it applies (output, the core's, then unused and
+// may be NULL), else as a launch of the linear kernels over output.
 int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const void* mask,
              void* output, void* stream, int row_stride, bool cfs = false,
-             const void* logits = nullptr) {
+             const void* logits = nullptr, const OutArgs* oa = nullptr) {
   Geometry g;
   int rc = validate(p, &g);
   if (rc != DCN_OK) return rc;
   if (row_stride && (row_stride < 3 * g.P || row_stride % 2)) return DCN_ERR_SHAPE;
   if (cfs && (p->stride_h != 1 || p->stride_w != 1 || g.Ho != p->H || g.Wo != p->W))
     return DCN_ERR_SHAPE;
+  if (oa && oa->n_out < 1) return DCN_ERR_SHAPE;
   if (g.units == 0) return DCN_OK;
-  if (!input || !offset || !mask || !output || (cfs && !logits)) return DCN_ERR_NULL;
+  if (!input || !offset || !mask || (!output && !oa) || (cfs && !logits) ||
+      (oa && (!oa->w || !oa->y)))
+    return DCN_ERR_NULL;
   const size_t es = (size_t)elem_size(p->dtype);
-  if (!aligned(input, es) || !aligned(mask, es) || !aligned(output, es) ||
-      !aligned(offset, 2 * es) || (cfs && !aligned(logits, es)))
+  if (!aligned(input, es) || !aligned(mask, es) || (output && !aligned(output, es)) ||
+      !aligned(offset, 2 * es) || (cfs && !aligned(logits, es)) ||
+      (oa && (!aligned(oa->w, es) || !aligned(oa->y, es) || (oa->bias && !aligned(oa->bias, es)))))
     return DCN_ERR_ALIGN;
   dcn::KParams kp;
   fill_kparams(p, g, &kp);
@@ -495,18 +509,42 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, kTileSmem,
                                              dcn::options().fwd_any_tile != 0);
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
+  // the projection in the epilogue, when there is no room for the core's
+  // output (with room, the two launches measure faster: the linear reads the
+  // output back from L2, while the epilogue's serial tail lengthens every
+  // block of the forward): 16-bit, separate tensors, 64 channels in one block
+  // (all groups), at most 64 tile pixels, n_out a multiple of 16 up to 128,
+  // weight and y 16-byte aligned
+  alignas(64) unsigned char wmap[128];
+  const bool fused_out =
+      oa && (dcn::options().fwd_out == 2 || (dcn::options().fwd_out == 1 && !output)) && tile &&
+      es == 2 && !row_stride &&
+      p->G * p->gc == 64 && tg.ngb == 1 && kp.tile_w * kp.tile_h <= 64 &&
+      (-cpt == 8 || -cpt == 16) && oa->n_out % 16 == 0 &&
+      oa->n_out <= 128 && aligned(oa->w, 16) && aligned(oa->y, 16) &&
+      dcn::encode_out_weight_map(p->dtype, oa->w, oa->n_out, wmap);
+  if (oa && !fused_out && !output) return DCN_ERR_UNSUPPORTED;  // nowhere to put the core's output
   if (fault_injected()) return DCN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool fused = cfs && tile && es == 2 && !row_stride && dcn::options().fwd_cfs;
+  const bool fused = cfs && tile && es == 2 && !row_stride && (dcn::options().fwd_cfs || fused_out);
   cudaError_t e =
       tile ? dcn::launch_fwd_tile(map, kp, tg, p->dtype, -cpt, input, offset, mask, output, st,
-                                  fused ? logits : nullptr)
+                                  fused ? logits : nullptr, fused_out ? wmap : nullptr,
+                                  fused_out ? oa->bias : nullptr, fused_out ? oa->y : nullptr,
+                                  fused_out ? oa->n_out : 0)
            : dcn::launch_fwd(kp, p->dtype, cpt, input, offset, mask, output, st);
   if (e == cudaSuccess && cfs && !fused) {
     const int gc = p->gc;
     e = dcn::launch_cfs_fwd(p->dtype, cfs_vbytes(gc, (int)es, false, {output, input, output}),
                             (long long)p->N * g.Ho * g.Wo, p->G * gc, p->G, output, input, logits,
                             output, st);
+  }
+  if (e == cudaSuccess && oa && !fused_out) {
+    const long long M = (long long)p->N * g.Ho * g.Wo;
+    const int C = p->G * p->gc;
+    const bool tc = dcn::options().linear_tc &&
+                    dcn::linear_tc_ok(p->dtype, M, C, oa->n_out, output, oa->w, oa->y);
+    e = dcn::launch_linear(p->dtype, M, C, oa->n_out, output, oa->w, oa->bias, oa->y, tc, st);
   }
   return finish(cuda_status(e), stream);
 }
@@ -523,6 +561,13 @@ int dcn_core_fwd(const dcn_params_t* p, const void* input, const void* offset, c
 int dcn_core_fwd_cfs(const dcn_params_t* p, const void* input, const void* offset,
                      const void* mask, const void* logits, void* output, void* stream) {
   return core_fwd(p, input, offset, mask, output, stream, 0, true, logits);
+}
+
+int dcn_core_fwd_out(const dcn_params_t* p, const void* input, const void* offset,
+                     const void* mask, const void* logits, const void* weight, const void* bias,
+                     int n_out, void* y, void* scratch, void* stream) {
+  const OutArgs oa{weight, bias, n_out, y};
+  return core_fwd(p, input, offset, mask, scratch, stream, 0, logits != nullptr, logits, &oa);
 }
 
 int dcn_core_fwd_om(const dcn_params_t* p, const void* input, const void* offset_mask,
@@ -906,6 +951,7 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_any_tile", &dcn::Options::fwd_any_tile},
     {"fwd_row64", &dcn::Options::fwd_row64},
     {"fwd_cfs", &dcn::Options::fwd_cfs},
+    {"fwd_out", &dcn::Options::fwd_out},
     {"fwd_proj", &dcn::Options::fwd_proj},
     {"fwd_proj_win", &dcn::Options::fwd_proj_win},
     {"fwd_proj_ws", &dcn::Options::fwd_proj_ws},

@@ -48,9 +48,17 @@ bool encode_input_map(const KParams& kp, const TileGeom& tg, int dtype, const vo
 // With logits (16-bit storage, separate offset / mask tensors, an output the
 // input's size at stride 1), the centre feature scale is applied before the
 // store (the fwd_tile_kernel CFS instance); cudaErrorInvalidValue otherwise.
+// With y, the output projection y = out W^T + bias runs in the epilogue
+// instead of the store of out (16-bit storage, separate tensors, 64 channels in
+// one block, at most 64 tile pixels, n_out a multiple of 16 up to 128; wmap
+// from encode_out_weight_map);
+// cudaErrorInvalidValue otherwise.
 cudaError_t launch_fwd_tile(const void* map, const KParams& kp, const TileGeom& tg, int dtype,
                             int cpt, const void* in, const void* off, const void* msk, void* out,
-                            cudaStream_t s, const void* logits = nullptr);
+                            cudaStream_t s, const void* logits = nullptr,
+                            const void* wmap = nullptr, const void* bias = nullptr,
+                            void* y = nullptr, int n_out = 0);
+bool encode_out_weight_map(int dtype, const void* w, int n_out, void* map_out);
 // Blocks whose bounded wait for a tensor copy ran out, since load.
 cudaError_t read_wait_timeouts(unsigned long long* count);
 // The CUDA driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000,

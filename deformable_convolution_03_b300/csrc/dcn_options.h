@@ -19,6 +19,7 @@ struct Options {
   int fwd_any_tile = 1;   // tiles of any shape (else powers of two) for the TMA forward
   int fwd_row64 = 1;      // 256-bit loads of merged 64-byte offset/mask rows
   int fwd_cfs = 1;        // the centre feature scale in the TMA forward's epilogue (else a second launch)
+  int fwd_out = 1;        // the output projection in the TMA forward's epilogue: 1 without scratch, 2 always, 0 never
   int fwd_proj = 1;       // the projection inside the forward: 1 without a rows buffer, 2 always, 0 never
   int fwd_proj_win = 40;  // window budget (KB) of the per-tile fused forward (40 measured fastest)
   int fwd_proj_ws = 1;    // the persistent, warp-specialised fused forward where it fits

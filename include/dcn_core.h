@@ -319,6 +319,34 @@ int dcn_center_feature_scale_bwd(const dcn_cfs_params_t* p, const void* grad_out
 int dcn_core_fwd_cfs(const dcn_params_t* p, const void* input, const void* offset,
                      const void* mask, const void* logits, void* output, void* stream);
 
+/* The core op followed by the module's output projection in one call (page
+ * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
+ * item 6: output_proj, a linear layer over the core's channels), optionally
+ * with the centre feature scale between them (logits non-NULL, as
+ * dcn_core_fwd_cfs):
+ *     y[n, ho, wo, :] = out[n, ho, wo, :] W^T + bias
+ * with out the core's (or the gate's) output rounded to the storage type, as
+ * dcn_core_fwd / dcn_core_fwd_cfs store it.
+ *   input, offset, mask   as dcn_core_fwd
+ *   logits                (N, H_out, W_out, G), or NULL for no gate
+ *   weight                (n_out, C) row-major; bias (n_out) or NULL
+ *   y                     (N, H_out, W_out, n_out), fully overwritten
+ *   scratch               (N, H_out, W_out, C) or NULL: room for out
+ * With scratch, out is written there and projected by the kernels of
+ * dcn_linear, which read it back from L2 (the faster way).  Without scratch,
+ * for float16 / bfloat16 with C = 64 (every channel of a pixel in one block of
+ * the tensor-copy forward), separate offset / mask tensors, n_out a multiple
+ * of 16 up to 128 and weight and y 16-byte aligned, one launch needs no room
+ * for out: the forward's epilogue runs the projection on the tensor cores
+ * (tcgen05); any other call without scratch returns DCN_ERR_UNSUPPORTED.
+ * Both ways take the same products of the same rounded values with float32
+ * sums.  No tensor may overlap another.
+ * Errors as dcn_core_fwd (and dcn_core_fwd_cfs with logits), plus
+ * DCN_ERR_SHAPE for n_out < 1 and DCN_ERR_NULL for weight or y. */
+int dcn_core_fwd_out(const dcn_params_t* p, const void* input, const void* offset,
+                     const void* mask, const void* logits, const void* weight, const void* bias,
+                     int n_out, void* y, void* scratch, void* stream);
+
 /* The feature step of the DCN module's offset branch (page
  * "没有CUDA内核也能跑：InternImage-G的DCNv3纯PyTorch回退实现逐行解读", section 三
  * item 2: the control features x1 from which the offset and mask projections
