@@ -65,28 +65,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "546140b8b796", "b9205b6706d6"
+_F, _B = "546140b8b796", "56900a5f393d"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_132_096, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 269_152_000, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_208_640, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_558_080, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_631_168, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_245_696, "sha": _B},
-    "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_836_928, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_041_728, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 268_238_336, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_297_728, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_440_064, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_691_584, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_133_056, "sha": _B},
+    "fwd@t_stage3_bf16": {"bytes": 17_317_376, "sha": _F},
+    "bwd@t_stage3_bf16": {"bytes": 23_807_744, "sha": _B},
     "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 11_940_864, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_715_904, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 311_057_920, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 63_263_232, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 301_410_816, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 73_114_624, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_196_544, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_064_320, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_596_544, "sha": _B},
+    "bwd@t_stage4_bf16": {"bytes": 11_940_608, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_497_280, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 309_824_512, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 62_977_792, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 298_326_528, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 73_680_128, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_385_728, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_541_504, "sha": _B},
 }
 
 
