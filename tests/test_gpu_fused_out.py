@@ -171,5 +171,12 @@ def test_argument_errors():
     assert e.value.status == B.DCN_ERR_SHAPE
 
 
+def test_empty_batch():
+    # no units: nothing is read or written, every pointer may be NULL
+    w = small("out_empty", "f16", gc=16, G=4, N=0)
+    B.dcn_core_fwd_out(lib_params(w), None, None, None, None,
+                       torch.empty(64, 64, dtype=torch.float16, device="cuda"), None, None)
+
+
 def test_no_wait_ran_out():
     assert B.dcn_wait_timeouts() == 0
