@@ -197,7 +197,7 @@ constexpr size_t kTileSmem = 64 * 1024;
 
 bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void* in,
                    dcn::KParams* kp, dcn::TileGeom* tg, void* map, size_t budget = kTileSmem,
-                   bool any_shape = false) {
+                   bool any_shape = false, int* halo = nullptr) {
   if (!dcn::options().fwd_tma) return false;
   const int es = elem_size(p->dtype);
   const long long C = (long long)p->G * p->gc;
@@ -276,6 +276,7 @@ bool plan_fwd_tile(const dcn_params_t* p, const Geometry& g, int cpt, const void
     kp->tile_h = bh;
     kp->tiles_w = (int)tiles_w;
     kp->tiles_h = (int)tiles_h;
+    if (halo) *halo = R;
     return dcn::encode_input_map(*kp, *tg, p->dtype, in, map);
   }
   return false;
@@ -506,8 +507,16 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   const int cpt = pick_fwd_cpt(p, g, input, output);
   alignas(64) unsigned char map[128];
   dcn::TileGeom tg;
-  const bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, kTileSmem,
-                                             dcn::options().fwd_any_tile != 0);
+  // a window whose halo within three blocks' shared memory is under 4 pixels
+  // (7 x 7 taps at stage 1: 3) takes up to two blocks' worth instead, so that
+  // fewer samples leave it for the far path (FlashInternImage-T stage 1, 7 x 7:
+  // 808 -> 573 us; 5 x 5, whose halo is 4, measured slower that way: 209 -> 221)
+  int halo = -1;
+  bool tile = cpt < 0 && plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, kTileSmem,
+                                       dcn::options().fwd_any_tile != 0, &halo);
+  const size_t big = (size_t)std::max(16, std::min(dcn::options().fwd_big_win, 200)) * 1024;
+  if (tile && halo < 4 && halo < dcn::options().fwd_halo && big > kTileSmem)
+    tile = plan_fwd_tile(p, g, -cpt, input, &kp, &tg, map, big, dcn::options().fwd_any_tile != 0);
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   // the projection in the epilogue, when there is no room for the core's
   // output (with room, the two launches measure faster: the linear reads the
@@ -948,6 +957,7 @@ constexpr OptionName kOptionNames[] = {
     {"fwd_tile", &dcn::Options::fwd_tile},
     {"fwd_tma", &dcn::Options::fwd_tma},
     {"fwd_halo", &dcn::Options::fwd_halo},
+    {"fwd_big_win", &dcn::Options::fwd_big_win},
     {"fwd_any_tile", &dcn::Options::fwd_any_tile},
     {"fwd_row64", &dcn::Options::fwd_row64},
     {"fwd_cfs", &dcn::Options::fwd_cfs},

@@ -16,6 +16,7 @@ struct Options {
   int fwd_tile = 1;       // 2-D pixel tiles for the wide kernel
   int fwd_tma = 1;        // the TMA-staged forward
   int fwd_halo = 6;       // largest halo of the TMA forward's window
+  int fwd_big_win = 112;  // window budget (KB) of the TMA forward when 64 KB leaves a halo under 4 (two blocks per SM)
   int fwd_any_tile = 1;   // tiles of any shape (else powers of two) for the TMA forward
   int fwd_row64 = 1;      // 256-bit loads of merged 64-byte offset/mask rows
   int fwd_cfs = 1;        // the centre feature scale in the TMA forward's epilogue (else a second launch)

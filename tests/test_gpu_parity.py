@@ -142,6 +142,18 @@ def test_tma_forward_instances(dt, gc, G, sm, rc, halo, opts):
     check_fwd(w, make_inputs(w))
 
 
+@pytest.mark.parametrize("k", [5, 7])
+@pytest.mark.parametrize("win_kb", [64, 112])
+def test_large_kernels_window_budget(k, win_kb, opts):
+    # 5 x 5 and 7 x 7 taps at FlashInternImage-T stage 1's plane (4 images):
+    # with 64 KB a 7 x 7 window keeps a halo of 3 and takes up to 112 KB
+    # instead; both budgets against the oracle, offsets N(0, 2)
+    opts.set("fwd_big_win", win_kb)
+    w = WORKLOADS["t_stage1_f16"].with_(name=f"t1_k{k}_{win_kb}", N=4, kernel_h=k, kernel_w=k,
+                                        pad_h=k // 2, pad_w=k // 2, P=k * k)
+    check_fwd(w, make_inputs(w))
+
+
 @pytest.mark.parametrize("geom", ["s2d2", "k5", "k7rc", "k1"])
 def test_tma_forward_geometries(geom):
     # windows for strided, dilated and larger kernels, and for 1x1
