@@ -102,6 +102,15 @@ def test_ragged_planes(dt, gc, G, sm, rc, opts):
     _check(w, 64, opts, seed=gc + G)
 
 
+@pytest.mark.parametrize("k", [5, 7])
+def test_large_kernels(k, opts):
+    # 5 x 5 and 7 x 7 taps (the 7 x 7 window takes the larger shared-memory
+    # budget, with the epilogue's operand tiles after it)
+    w = small(f"out_k{k}", "f16", gc=16, G=4, N=2, H=13, W=11, kernel_h=k, kernel_w=k,
+              pad_h=k // 2, pad_w=k // 2, softmax=1)
+    _check(w, 64, opts, seed=k)
+
+
 def test_many_tiles_per_sm(opts):
     # 64 images of 56 x 56: every SM runs many blocks, each allocating and
     # freeing its tensor memory
