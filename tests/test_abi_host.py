@@ -123,6 +123,32 @@ def test_null_arguments(native):
 
 
 @host_only
+def test_fused_forward_argument_errors(native):
+    # dcn_core_fwd_cfs / dcn_core_fwd_out: every check that precedes the first
+    # CUDA call
+    lib = native.lib()
+    p = native.Params(N=1, H=8, W=8, G=4, gc=16, dtype=native.DCN_F16)
+    pp = ctypes.byref(p.c())
+    cfs, out = lib.dcn_core_fwd_cfs, lib.dcn_core_fwd_out
+    assert cfs(None, A, A, A, A, A, None) == native.DCN_ERR_NULL
+    assert cfs(pp, A, A, A, None, A, None) == native.DCN_ERR_NULL  # the logits
+    assert cfs(pp, A, A, A, A + 1, A, None) == native.DCN_ERR_ALIGN
+    s2 = native.Params(N=1, H=8, W=8, G=4, gc=16, dtype=native.DCN_F16, stride_h=2, stride_w=2)
+    assert cfs(ctypes.byref(s2.c()), A, A, A, A, A, None) == native.DCN_ERR_SHAPE
+    assert out(None, A, A, A, None, A, None, 64, A, None, None) == native.DCN_ERR_NULL
+    assert out(pp, A, A, A, None, A, None, 0, A, None, None) == native.DCN_ERR_SHAPE
+    assert out(pp, A, A, A, None, None, None, 64, A, None, None) == native.DCN_ERR_NULL
+    assert out(pp, A, A, A, None, A, None, 64, None, None, None) == native.DCN_ERR_NULL
+    assert out(pp, A, A, A, None, A + 1, None, 64, A, None, None) == native.DCN_ERR_ALIGN
+    assert out(pp, A, A, A, None, A, A + 1, 64, A, None, None) == native.DCN_ERR_ALIGN
+    assert out(ctypes.byref(s2.c()), A, A, A, A, A, None, 64, A, None, None) == native.DCN_ERR_SHAPE
+    # no units: nothing to do, nothing touched
+    e = native.Params(N=0, H=8, W=8, G=4, gc=16, dtype=native.DCN_F16)
+    assert out(ctypes.byref(e.c()), None, None, None, None, A, None, 64, None, None,
+               None) == native.DCN_OK
+
+
+@host_only
 def test_misaligned_pointers(native):
     lib = native.lib()
     for dtype, es in ((native.DCN_F32, 4), (native.DCN_F16, 2), (native.DCN_BF16, 2)):
