@@ -61,32 +61,33 @@ FALLBACK_HBM_GBS = 6400.0
 # DRAM traffic per call (dram__bytes_read.sum + dram__bytes_write.sum of the
 # call's kernels in an ncu capture of `bench.py --profile-step --workload W`),
 # keyed by phase and workload, with the sha1 of the kernel sources it was
-# taken on: a changed source voids the figure.  The backward's memset of its
+# taken on (the kernels' and the planner's, with the switches' defaults): a
+# changed source voids the figure.  The backward's memset of its
 # float32 accumulator is not a kernel and is not counted.
-FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh")
-BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh")
-_F, _B = "546140b8b796", "56900a5f393d"
+FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
+BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
+_F, _B = "317d99c1b533", "20d5afb3e0e6"
 TRAFFIC = {
-    "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
+    "fwd@v3_tiny_f32": {"bytes": 60_416, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_041_728, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 268_238_336, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_297_728, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 268_440_064, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_691_584, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_133_056, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_059_392, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 268_920_320, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_206_080, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 269_114_624, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_637_568, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_206_528, "sha": _B},
     "fwd@t_stage3_bf16": {"bytes": 17_317_376, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_807_744, "sha": _B},
-    "fwd@t_stage4_bf16": {"bytes": 8_686_848, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 11_940_608, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_497_280, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 309_824_512, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 62_977_792, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 298_326_528, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 73_680_128, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_385_728, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_059_712, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_541_504, "sha": _B},
+    "bwd@t_stage3_bf16": {"bytes": 23_838_464, "sha": _B},
+    "fwd@t_stage4_bf16": {"bytes": 8_687_104, "sha": _F},
+    "bwd@t_stage4_bf16": {"bytes": 11_940_352, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_652_672, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 309_710_336, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 62_963_456, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 298_332_160, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 72_869_888, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_393_664, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_063_552, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_621_120, "sha": _B},
 }
 
 

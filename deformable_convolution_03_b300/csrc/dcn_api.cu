@@ -307,7 +307,7 @@ int pick_bwd_cpt(const dcn_params_t* p, const void* in, const void* gout, const 
 // over windows, one thread per output pixel of a TH x TW <= 256 tile of one
 // (image, group).  Of the tile shapes, the one with the least work (tiles x
 // (256 threads + window pixels)) is taken; the window is the tile's footprint
-// plus a halo of R pixels for the offsets, R from 6 (the bwd_halo switch) down to 1
+// plus a halo of R pixels for the offsets, R from 5 (the bwd_halo switch) down to 1
 // so that the shared memory stays within kSplitSmem (four CTAs per SM).
 // Needs gc*es of 16, 32 or 64 bytes, P <= 16, grad_out 32-byte aligned (16 for
 // 16-byte rows) and the float32 accumulator 16-byte aligned.  Returns the
