@@ -720,10 +720,12 @@ int dwconv_plan(const dcn_dwconv_params_t* p, const void* x, const void* w, cons
     int np0 = std::max(1, 128 / (p->C / 2));  // 128 threads measured faster than 256
     if (o.dw_patches > 0) np0 = std::min(o.dw_patches, std::max(1, 256 / (p->C / 2)));
     np0 = 1 << (31 - __builtin_clz((unsigned)np0));  // a power of two
-    // 4-row patches first (fewer footprint reads per output), then 2-row
-    for (const size_t cap : {kDwSmemTwo, kDwSmemOne}) {
-      for (const int py : {4, 2}) {
-        if (o.dw_py && py != o.dw_py) continue;
+    // 4-row patches first (fewer footprint reads per output), then 2-row;
+    // each at two blocks per SM, else one (4-row patches at one block per SM
+    // beat 2-row at two: InternImage-G stage 1, C = 512, 61.6 -> 59.4 us)
+    for (const int py : {4, 2}) {
+      if (o.dw_py && py != o.dw_py) continue;
+      for (const size_t cap : {kDwSmemTwo, kDwSmemOne}) {
         for (int np = np0; np >= 1 && !d->tiled; np /= 2) {
           d->ph = np >= 4 ? 2 : 1;
           d->pw = np / d->ph;
