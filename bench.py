@@ -66,28 +66,28 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
-_F, _B = "317d99c1b533", "20d5afb3e0e6"
+_F, _B = "1aeaa7b81981", "65c11bec2039"
 TRAFFIC = {
-    "fwd@v3_tiny_f32": {"bytes": 60_416, "sha": _F},
+    "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},
-    "fwd@t_stage1_f16": {"bytes": 72_059_392, "sha": _F},
-    "bwd@t_stage1_f16": {"bytes": 268_920_320, "sha": _B},
-    "fwd@t_stage1_bf16": {"bytes": 72_206_080, "sha": _F},
-    "bwd@t_stage1_bf16": {"bytes": 269_114_624, "sha": _B},
-    "fwd@t_stage2_bf16": {"bytes": 34_637_568, "sha": _F},
-    "bwd@t_stage2_bf16": {"bytes": 105_206_528, "sha": _B},
-    "fwd@t_stage3_bf16": {"bytes": 17_317_376, "sha": _F},
-    "bwd@t_stage3_bf16": {"bytes": 23_838_464, "sha": _B},
+    "fwd@t_stage1_f16": {"bytes": 72_210_176, "sha": _F},
+    "bwd@t_stage1_f16": {"bytes": 269_116_160, "sha": _B},
+    "fwd@t_stage1_bf16": {"bytes": 72_225_024, "sha": _F},
+    "bwd@t_stage1_bf16": {"bytes": 268_785_664, "sha": _B},
+    "fwd@t_stage2_bf16": {"bytes": 34_699_008, "sha": _F},
+    "bwd@t_stage2_bf16": {"bytes": 105_152_512, "sha": _B},
+    "fwd@t_stage3_bf16": {"bytes": 17_317_120, "sha": _F},
+    "bwd@t_stage3_bf16": {"bytes": 23_797_504, "sha": _B},
     "fwd@t_stage4_bf16": {"bytes": 8_687_104, "sha": _F},
-    "bwd@t_stage4_bf16": {"bytes": 11_940_352, "sha": _B},
-    "fwd@g_stage1_bf16": {"bytes": 66_652_672, "sha": _F},
-    "bwd@g_stage1_bf16": {"bytes": 309_710_336, "sha": _B},
-    "fwd@g_stage1_rc_bf16": {"bytes": 62_963_456, "sha": _F},
-    "bwd@g_stage1_rc_bf16": {"bytes": 298_332_160, "sha": _B},
-    "fwd@fb28_f32": {"bytes": 72_869_888, "sha": _F},
-    "bwd@fb28_f32": {"bytes": 153_393_664, "sha": _B},
-    "fwd@fb28_s2d2_f32": {"bytes": 35_063_552, "sha": _F},
-    "bwd@fb28_s2d2_f32": {"bytes": 67_621_120, "sha": _B},
+    "bwd@t_stage4_bf16": {"bytes": 11_940_608, "sha": _B},
+    "fwd@g_stage1_bf16": {"bytes": 66_867_456, "sha": _F},
+    "bwd@g_stage1_bf16": {"bytes": 309_864_192, "sha": _B},
+    "fwd@g_stage1_rc_bf16": {"bytes": 62_951_936, "sha": _F},
+    "bwd@g_stage1_rc_bf16": {"bytes": 298_695_424, "sha": _B},
+    "fwd@fb28_f32": {"bytes": 72_508_928, "sha": _F},
+    "bwd@fb28_f32": {"bytes": 153_240_576, "sha": _B},
+    "fwd@fb28_s2d2_f32": {"bytes": 35_062_272, "sha": _F},
+    "bwd@fb28_s2d2_f32": {"bytes": 67_902_208, "sha": _B},
 }
 
 
