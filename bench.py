@@ -66,7 +66,7 @@ FALLBACK_HBM_GBS = 6400.0
 # float32 accumulator is not a kernel and is not counted.
 FWD_SRCS = ("dcn_fwd_tma.cu", "dcn_fwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
 BWD_SRCS = ("dcn_bwd_split.cu", "dcn_bwd.cu", "dcn_common.cuh", "dcn_api.cu", "dcn_options.h")
-_F, _B = "1aeaa7b81981", "65c11bec2039"
+_F, _B = "194dd595571d", "8ef9c1baf1f9"
 TRAFFIC = {
     "fwd@v3_tiny_f32": {"bytes": 60_160, "sha": _F},
     "bwd@v3_tiny_f32": {"bytes": 51_968, "sha": _B},

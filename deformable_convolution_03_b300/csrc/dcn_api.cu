@@ -520,8 +520,8 @@ int core_fwd(const dcn_params_t* p, const void* input, const void* offset, const
   if (cpt < 0 && !tile) plan_fwd_tiles(p, g, -cpt, &kp);
   // the projection in the epilogue, when there is no room for the core's
   // output (with room, the two launches measure faster: the linear reads the
-  // output back from L2, while the epilogue's serial tail lengthens every
-  // block of the forward): 16-bit, separate tensors, 64 channels in one block
+  // output back from L2, while the epilogue's work lengthens every block of a
+  // forward that is bound by instruction issue): 16-bit, separate tensors, 64 channels in one block
   // (all groups), at most 64 tile pixels, n_out a multiple of 16 up to 128,
   // weight and y 16-byte aligned
   alignas(64) unsigned char wmap[128];
